@@ -1,0 +1,409 @@
+"""Benchmark: sparse-attention forward query-tokens/s on the model-shape workload.
+
+One step = the forward of all 16 layers of B=32 sequences of T=1024 tokens
+(W=12, linear stagger alpha_l = 0.5 + l/15, Fibonacci base, bf16, 8 query / 2
+key-value heads, d=64), each layer its own seeded inputs already resident in
+HBM.  The 16 layers' inputs (1.34 GB) are larger than L2, so no flush is
+needed between steps.  ``value`` counts query tokens of every layer call.
+
+Also reported: ``e2e`` (the same step through the C ABI with pinned host
+buffers, host->device inputs and device->host outputs inside the timed
+region), ``roofline`` (the forward kernel's ideal bytes -- one read of Q, K, V
+and one write of O -- over its average launch time from CUDA events on its
+stream, against the measured HBM copy bandwidth), ``cpu_baseline`` (the fp64
+CPU oracle on a bounded sample), and SM clocks sampled during the timed
+region.
+
+``--impl reference`` times the CPU oracle itself as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn fwd query-tokens/s (T=1024,W=12,bf16); HBM GB/s as % of GB300 peak"
+UNIT = "query-tokens/s"
+IDEAL_BYTES_PER_TOKEN = 2 * (8 * 64 + 2 * 64 + 2 * 64 + 8 * 64)  # bf16 Q, K, V read + O write
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="model-shape",
+                    choices=["model-shape", "extrapolation", "pow2", "train-step", "long-forward"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload_of(name):
+    from fibonacci_spaced_sparse_gb300 import workloads as w
+    return {"model-shape": w.MODEL_SHAPE, "extrapolation": w.EXTRAPOLATION, "pow2": w.POW2,
+            "train-step": w.TRAIN_STEP, "long-forward": w.LONG_FORWARD}[name]
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured (copy test)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------- traffic record --
+
+def kernel_source_digest():
+    from fibonacci_spaced_sparse_gb300 import build
+    h = hashlib.sha256()
+    for p in sorted(build.sources()):
+        with open(p, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_name):
+    """DRAM bytes per launch of the forward kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"fwd_{workload_name}_traffic.txt")
+    try:
+        kv = {}
+        with open(path) as fh:
+            for line in fh:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_digest") != kernel_source_digest():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------- CPU baseline --
+
+def cpu_baseline(wl, budget_s=12.0):
+    """The fp64 oracle as it stands on the host cores: whole layers of the
+    workload (all B sequences), layer after layer, until the budget is spent."""
+    import torch
+    from fibonacci_spaced_sparse_gb300 import inputs
+    from oracle import oracle
+    oracle.build()
+    alphas, _ = wl.alphas()
+    cores = oracle.default_threads()
+    tokens, spent, layers = 0, 0.0, 0
+    for l in range(wl.layers):
+        x = inputs.qkv(wl.B, wl.T, dtype=torch.bfloat16, layer=l)
+        f = {k: v.to(torch.float64).numpy() for k, v in x.items()}
+        t0 = time.perf_counter()
+        oracle.forward(f["q"], f["k"], f["v"], W=wl.window(l), rungs=wl.rungs(), alpha=alphas[l],
+                       nthreads=cores)
+        spent += time.perf_counter() - t0
+        tokens += wl.B * wl.T
+        layers += 1
+        if spent >= budget_s:
+            break
+    return {"value": tokens / spent, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{layers} of {wl.layers} layers, all {wl.B}x{wl.T} query tokens each, "
+                      f"{spent:.1f} s"}
+
+
+# --------------------------------------------------------------- our arm --
+
+def run_ours(args, rank, world, local):
+    import torch
+    from fibonacci_spaced_sparse_gb300 import api, inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload_of(args.workload)
+    alphas, _ = wl.alphas()
+    L = wl.layers
+    bf = torch.bfloat16
+    # every rank holds its own batch (weak scaling: replicas over independent sequences)
+    host = [inputs.qkv(wl.B, wl.T, dtype=bf, seed=42 + 1000 * rank, layer=l, with_dO=wl.backward)
+            for l in range(L)]
+    dv = [{k: v.to(dev) for k, v in h.items()} for h in host]
+    outs = [torch.empty_like(d["q"]) for d in dv]
+    lses = [torch.empty((wl.B, wl.T, 8), dtype=torch.float32, device=dev) for _ in range(L)]
+    api.rope_table(wl.T, dev)
+    stream = torch.cuda.current_stream(dev)
+    ws = None
+    if wl.backward:
+        need = max(api.sfa_backward_workspace_size(wl.B, wl.T, alpha=a, W=wl.window(l),
+                                                   rungs=wl.rungs()) for l, a in enumerate(alphas))
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+    def step(events=None):
+        for l in range(L):
+            if events is not None:
+                events[l][0].record(stream)
+            api.sfa_forward(dv[l]["q"], dv[l]["k"], dv[l]["v"], alpha=alphas[l], W=wl.window(l),
+                            rungs=wl.rungs(), out=outs[l], lse=lses[l])
+            if events is not None:
+                events[l][1].record(stream)
+            if wl.backward:
+                api.sfa_backward(dv[l]["q"], dv[l]["k"], dv[l]["v"], outs[l], dv[l]["dO"], lses[l],
+                                 alpha=alphas[l], W=wl.window(l), rungs=wl.rungs(), workspace=ws)
+
+    use_dist = world > 1
+    if use_dist:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if use_dist:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+
+    # device-timed region: K steps, per-launch events on the launching stream
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
+          for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = api.launch_count()
+    with ClockSampler(local) as clk:
+        barrier()
+        start.record(stream)
+        for s in range(args.steps):
+            step(ev[s])
+        stop.record(stream)
+        barrier()
+    launches = api.launch_count() - n0
+    elapsed_ms = start.elapsed_time(stop)
+    fwd_ms = [e[0].elapsed_time(e[1]) for st in ev for e in st]
+    if use_dist:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    tokens = wl.B * wl.T * L * args.steps * world
+    value = tokens / (elapsed_ms / 1e3)
+
+    # roofline of the forward kernel
+    peak, peak_kind = measured_peak()
+    avg_launch_s = statistics.mean(fwd_ms) / 1e3
+    ideal = IDEAL_BYTES_PER_TOKEN * wl.B * wl.T
+    achieved = ideal / avg_launch_s / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    # end to end through the C ABI with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, alphas, host, dev, stream, world, use_dist)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu and world == 1:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "W": list(wl.W),
+                       "layers": L, "schedule": wl.schedule, "base": wl.base,
+                       "heads": "8q/2kv", "head_dim": 64,
+                       "backward": wl.backward,
+                       "l2": f"inputs larger than L2 ({L * 50.3 * wl.tokens / 32768:.0f} MB of "
+                             "Q/K/V per step), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "forward", "ideal_bytes_per_launch": ideal,
+                         "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if use_dist:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
+    """Same step through the C ABI from pinned host buffers: each step copies
+    every layer's Q, K, V host->device, runs the layer, and copies O back."""
+    import torch
+    from fibonacci_spaced_sparse_gb300 import api
+    L = wl.layers
+    pin = [{k: host[l][k].pin_memory() for k in ("q", "k", "v")} for l in range(L)]
+    o_host = [torch.empty_like(pin[l]["q"]).pin_memory() for l in range(L)]
+    dq = [{k: torch.empty_like(pin[l][k], device=dev) for k in ("q", "k", "v")} for l in range(L)]
+    do = [torch.empty_like(dq[l]["q"]) for l in range(L)]
+    lse = [torch.empty((wl.B, wl.T, 8), dtype=torch.float32, device=dev) for _ in range(L)]
+    h2d = sum(pin[l][k].numel() * pin[l][k].element_size() for l in range(L) for k in pin[l])
+    d2h = sum(o.numel() * o.element_size() for o in o_host)
+
+    def step():
+        for l in range(L):
+            for k in ("q", "k", "v"):
+                dq[l][k].copy_(pin[l][k], non_blocking=True)
+            api.sfa_forward(dq[l]["q"], dq[l]["k"], dq[l]["v"], alpha=alphas[l], W=wl.window(l),
+                            rungs=wl.rungs(), out=do[l], lse=lse[l])
+            o_host[l].copy_(do[l], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        step()
+    stop.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = start.elapsed_time(stop)
+    if use_dist:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens = wl.B * wl.T * L * args.steps * world
+    return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+# --------------------------------------------------------- reference arm --
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm: each step is one whole layer of the
+    workload (B x T query tokens) on all host cores."""
+    if rank != 0:
+        return
+    import torch
+    from fibonacci_spaced_sparse_gb300 import inputs
+    from oracle import oracle
+    oracle.build()
+    wl = workload_of(args.workload)
+    alphas, _ = wl.alphas()
+    cores = oracle.default_threads()
+    data = []
+    for l in range(min(wl.layers, args.steps + max(3, args.warmup))):
+        x = inputs.qkv(wl.B, wl.T, dtype=torch.bfloat16, layer=l)
+        data.append({k: v.to(torch.float64).numpy() for k, v in x.items()})
+
+    def step(i):
+        l = i % len(data)
+        f = data[l]
+        oracle.forward(f["q"], f["k"], f["v"], W=wl.window(l), rungs=wl.rungs(), alpha=alphas[l],
+                       nthreads=cores)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    tokens = wl.B * wl.T * args.steps
+    value = tokens / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "W": list(wl.W),
+                   "layers": wl.layers, "schedule": wl.schedule, "base": wl.base},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"one whole layer ({wl.B}x{wl.T} query tokens) per step"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    from fibonacci_spaced_sparse_gb300 import build
+    build.build()
+    run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

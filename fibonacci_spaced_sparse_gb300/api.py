@@ -1,0 +1,228 @@
+"""Python binding of libsfa: the C ABI calls with the same names, over torch
+tensors.  Argument marshalling only -- every step of the attention runs in the
+library's CUDA kernels; torch supplies device memory and streams.
+
+Method: "Depth-Staggered Fibonacci Spacing for Sparse Attention: Static
+Schedules Beat Learned Dilation and Extrapolate Where Dense Attention Fails"
+(arXiv 2606.28560), section 2 "Method".
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Sequence
+
+import torch
+
+from . import _lib
+
+FIBONACCI_BASE = (1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987)
+"""Section 2 "Attended set": the base offsets f_k, K = 15."""
+
+
+def pow2_base(T: int) -> tuple:
+    """Section 2 "Control base": the reach-matched power-of-two base, every
+    2^k below the sequence length T (K = 10 at T = 1024)."""
+    out, x = [], 1
+    while x < T:
+        out.append(x)
+        x *= 2
+    return tuple(out)
+
+
+_DTYPES = {torch.float32: _lib.SFA_F32, torch.bfloat16: _lib.SFA_BF16}
+
+
+def _vp(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(device, stream=None) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Params:
+    """An sfa_params struct plus the host rung array it points to."""
+
+    def __init__(self, B, T, *, W, alpha, rungs=FIBONACCI_BASE, rope_theta=1e4, scale=0.0,
+                 dtype=torch.bfloat16, Hq=8, Hkv=2, D=64):
+        self._rungs = (ctypes.c_float * max(1, len(rungs)))(*[float(f) for f in rungs])
+        p = _lib.SfaParams()
+        p.B, p.T, p.Hq, p.Hkv, p.D = int(B), int(T), int(Hq), int(Hkv), int(D)
+        p.W, p.K = int(W), len(rungs)
+        p.rungs = ctypes.cast(self._rungs, ctypes.POINTER(ctypes.c_float))
+        p.alpha = float(alpha)
+        p.rope_theta = float(rope_theta)
+        p.scale = float(scale)
+        if dtype not in _DTYPES:
+            raise TypeError(f"unsupported dtype {dtype}")
+        p.dtype = _DTYPES[dtype]
+        self.struct = p
+
+    def ref(self):
+        return ctypes.byref(self.struct)
+
+
+# ------------------------------------------------------- host-side helpers --
+
+
+def alpha_from_theta(theta: float) -> float:
+    """alpha = 0.5 + sigmoid(theta) (section 2 "Per-layer scalar")."""
+    return float(_lib.load().sfa_alpha_from_theta(float(theta)))
+
+
+def alpha_schedule(kind: str, L: int = 16, S: int = 7, thetas: Sequence[float] | None = None) -> list:
+    """Per-layer alphas of the fixed, learned, linear or coprime schedule."""
+    lib = _lib.load()
+    out = (ctypes.c_float * L)()
+    th = (ctypes.c_float * L)(*[float(t) for t in thetas]) if thetas is not None else None
+    st = lib.sfa_alpha_schedule(_lib.SCHEDULES[kind], int(L), int(S),
+                                ctypes.cast(th, ctypes.POINTER(ctypes.c_float)) if th else None,
+                                ctypes.cast(out, ctypes.POINTER(ctypes.c_float)))
+    _lib.check(st, "sfa_alpha_schedule")
+    return [float(x) for x in out]
+
+
+def rung_plan(*, T: int, W: int, alpha: float, rungs=FIBONACCI_BASE, B: int = 1):
+    """The rungs the kernels use: list of (index, floor d, t, ceil d)."""
+    lib = _lib.load()
+    p = Params(B, T, W=W, alpha=alpha, rungs=rungs)
+    K = max(1, len(rungs))
+    n = ctypes.c_int(0)
+    idx, fl, ce = (ctypes.c_int * K)(), (ctypes.c_int * K)(), (ctypes.c_int * K)()
+    fr = (ctypes.c_float * K)()
+    st = lib.sfa_rung_plan(p.ref(), ctypes.byref(n), idx, fl, fr, ce)
+    _lib.check(st, "sfa_rung_plan")
+    return [(idx[i], fl[i], float(fr[i]), ce[i]) for i in range(n.value)]
+
+
+def launch_count() -> int:
+    return int(_lib.load().sfa_launch_count())
+
+
+# ------------------------------------------------------------- RoPE table --
+
+_rope_cache: dict = {}
+
+
+def rope_table(T: int, device, D: int = 64, rope_theta: float = 1e4, stream=None) -> torch.Tensor:
+    """Device RoPE table [T, D/2, 2] (cos, sin), built once per (device, D,
+    theta) and grown on demand; any table with >= T rows serves length T."""
+    device = torch.device(device)
+    key = (device.index if device.index is not None else torch.cuda.current_device(), D,
+           float(rope_theta))
+    tab = _rope_cache.get(key)
+    if tab is None or tab.shape[0] < T:
+        rows = max(T, 1024 if tab is None else 2 * tab.shape[0])
+        lib = _lib.load()
+        n = lib.sfa_rope_table_floats(int(rows), int(D))
+        tab = torch.empty(n, dtype=torch.float32, device=device).view(rows, D // 2, 2)
+        st = lib.sfa_rope_table(_vp(tab), int(rows), int(D), float(rope_theta), _stream(device, stream))
+        _lib.check(st, "sfa_rope_table")
+        # the table is shared by later calls on any stream: finish building it
+        (stream if stream is not None else torch.cuda.current_stream(device)).synchronize()
+        _rope_cache[key] = tab
+    return tab
+
+
+# -------------------------------------------------------- forward/backward --
+
+
+def _check_qkv(q, k, v):
+    for name, t, H in (("q", q, 8), ("k", k, 2), ("v", v, 2)):
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if t.dim() != 4 or t.shape[2] != H or t.shape[3] != 64:
+            raise ValueError(f"{name} must be [B, T, {H}, 64], got {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.dtype != q.dtype:
+            raise ValueError("q, k, v must share a dtype")
+    if k.shape[:2] != q.shape[:2] or v.shape[:2] != q.shape[:2]:
+        raise ValueError("q, k, v must share B and T")
+
+
+def sfa_forward(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE, rope_theta: float = 1e4,
+                scale: float = 0.0, need_lse: bool = True, out=None, lse=None, status=None,
+                stream=None):
+    """O (and LSE) of the sparse attention for one layer; see include/sfa.h."""
+    _check_qkv(q, k, v)
+    B, T = q.shape[0], q.shape[1]
+    o = out if out is not None else torch.empty_like(q)
+    if need_lse and lse is None:
+        lse = torch.empty((B, T, 8), dtype=torch.float32, device=q.device)
+    p = Params(B, T, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
+               dtype=q.dtype)
+    tab = rope_table(T, q.device, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
+    st = _lib.load().sfa_forward(p.ref(), _vp(q), _vp(k), _vp(v), _vp(tab), _vp(o),
+                                 _vp(lse if need_lse else None), _vp(status),
+                                 _stream(q.device, stream))
+    _lib.check(st, "sfa_forward")
+    return o, (lse if need_lse else None)
+
+
+def sfa_backward_workspace_size(B: int, T: int, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
+                                dtype=torch.bfloat16) -> int:
+    p = Params(B, T, W=W, alpha=alpha, rungs=rungs, dtype=dtype)
+    return int(_lib.load().sfa_backward_workspace_size(p.ref()))
+
+
+def sfa_backward(q, k, v, o, dO, lse, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
+                 rope_theta: float = 1e4, scale: float = 0.0, workspace=None, status=None,
+                 stream=None):
+    """(dQ, dK, dV, dalpha, dtheta) of the sparse attention; dalpha/dtheta are
+    one-element fp32 device tensors."""
+    _check_qkv(q, k, v)
+    B, T = q.shape[0], q.shape[1]
+    for name, t in (("o", o), ("dO", dO)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError(f"{name} must match q")
+    p = Params(B, T, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
+               dtype=q.dtype)
+    lib = _lib.load()
+    need = int(lib.sfa_backward_workspace_size(p.ref()))
+    if workspace is None or workspace.numel() < need:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    da = torch.empty(1, dtype=torch.float32, device=q.device)
+    dth = torch.empty(1, dtype=torch.float32, device=q.device)
+    tab = rope_table(T, q.device, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
+    st = lib.sfa_backward(p.ref(), _vp(q), _vp(k), _vp(v), _vp(o), _vp(dO), _vp(lse), _vp(tab),
+                          _vp(dq), _vp(dk), _vp(dv), _vp(da), _vp(dth), _vp(workspace),
+                          ctypes.c_size_t(workspace.numel()), _vp(status),
+                          _stream(q.device, stream))
+    _lib.check(st, "sfa_backward")
+    return dq, dk, dv, da, dth
+
+
+def sfa_read_status(status: torch.Tensor, stream=None) -> int:
+    """Synchronises and returns the device status word (0 = no error)."""
+    w = ctypes.c_uint(0)
+    st = _lib.load().sfa_read_status(_vp(status), ctypes.byref(w), _stream(status.device, stream))
+    if st not in (_lib.SFA_OK, _lib.SFA_ERR_DEVICE_STATUS):
+        _lib.check(st, "sfa_read_status")
+    return int(w.value)
+
+
+class SparseAttention(torch.autograd.Function):
+    """Autograd wrapper: o = attention(q, k, v; alpha = 0.5 + sigmoid(theta)).
+
+    theta is a 0-d tensor (the layer's only added parameter); its gradient is
+    the library's dtheta."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, theta, W, rungs=FIBONACCI_BASE, rope_theta=1e4):
+        alpha = alpha_from_theta(float(theta))
+        o, lse = sfa_forward(q, k, v, alpha=alpha, W=W, rungs=rungs, rope_theta=rope_theta)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.cfg = (alpha, W, tuple(rungs), rope_theta)
+        return o
+
+    @staticmethod
+    def backward(ctx, dO):
+        q, k, v, o, lse = ctx.saved_tensors
+        alpha, W, rungs, rope_theta = ctx.cfg
+        dq, dk, dv, _, dth = sfa_backward(q, k, v, o, dO.contiguous(), lse, alpha=alpha, W=W,
+                                          rungs=rungs, rope_theta=rope_theta)
+        return dq, dk, dv, dth.reshape(()), None, None, None

@@ -1,0 +1,257 @@
+// sfa_api.cu -- the C ABI of libsfa (declared in include/sfa.h): argument
+// validation, the per-layer rung preparation, and kernel dispatch.
+//
+// Method: "Depth-Staggered Fibonacci Spacing for Sparse Attention"
+// (arXiv 2606.28560), section 2 "Method" -- the attended set (window 0..W plus
+// rungs at d_k = alpha f_k read by interpolation) and the per-layer scalar
+// alpha = 0.5 + sigmoid(theta).
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "sfa.h"
+#include "sfa_internal.cuh"
+
+namespace sfa {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace sfa
+
+using sfa::LayerArgs;
+using sfa::Rung;
+
+namespace {
+
+constexpr int kMaxT = 1 << 24;  // positions stay exact in fp32
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape and value checks shared by every entry point.
+sfa_status validate(const sfa_params* p) {
+    if (!p) return SFA_ERR_INVALID_ARG;
+    if (p->B < 0 || p->T < 0 || p->Hq <= 0 || p->Hkv <= 0 || p->D <= 0 || p->W < 0)
+        return SFA_ERR_INVALID_ARG;
+    if (p->K < 0 || p->K > SFA_MAX_RUNGS || (p->K > 0 && !p->rungs)) return SFA_ERR_INVALID_ARG;
+    for (int k = 0; k < p->K; ++k)
+        if (!std::isfinite(p->rungs[k]) || !(p->rungs[k] > 0.f)) return SFA_ERR_INVALID_ARG;
+    if (!std::isfinite(p->alpha) || !(p->alpha > 0.f)) return SFA_ERR_INVALID_ARG;
+    if (!std::isfinite(p->rope_theta) || !std::isfinite(p->scale) || p->scale < 0.f)
+        return SFA_ERR_INVALID_ARG;
+    if (p->dtype != SFA_F32 && p->dtype != SFA_BF16) return SFA_ERR_INVALID_ARG;
+    if (p->Hq != sfa::kHq || p->Hkv != sfa::kHkv || p->D != sfa::kD) return SFA_ERR_UNSUPPORTED;
+    if (p->T > kMaxT || (long long)p->B * p->T > 0x7fffffffLL) return SFA_ERR_UNSUPPORTED;
+    return SFA_OK;
+}
+
+// Rung preparation ("Attended set"): d = fl32(alpha) * fl32(f) rounded to
+// nearest; rungs with d <= W are dropped (inside the window); rungs whose
+// ceil(d) exceeds T - 1 are masked for every query and are left out too.
+int rung_plan(const sfa_params* p, Rung* out) {
+    int n = 0;
+    for (int k = 0; k < p->K; ++k) {
+        volatile float d = p->alpha * p->rungs[k];
+        const float dv = d;
+        if (!(dv > (float)p->W)) continue;
+        if (dv >= (float)p->T) continue;  // ceil(d) >= T: masked for all i < T
+        const float fl = std::floor(dv);
+        const float ce = std::ceil(dv);
+        if ((int)ce > p->T - 1) continue;
+        Rung r;
+        r.n = (int)fl;
+        r.t = dv - fl;  // exact: fl and dv share the exponent range
+        r.c = (int)ce;
+        r.f = p->rungs[k];
+        r.index = k;
+        out[n++] = r;
+    }
+    return n;
+}
+
+void fill_args(const sfa_params* p, LayerArgs* a) {
+    std::memset(a, 0, sizeof(*a));
+    a->B = p->B;
+    a->T = p->T;
+    a->W = p->W;
+    a->scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt((float)p->D);
+    a->alpha = p->alpha;
+    a->nr = rung_plan(p, a->r);
+}
+
+const float2* rope_ptr(const sfa_params* p, const float* table) {
+    return p->rope_theta > 0.f ? reinterpret_cast<const float2*>(table) : nullptr;
+}
+
+sfa_status launched(cudaError_t e) {
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
+    return SFA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+SFA_API int sfa_version(void) { return (1 << 16) | 0; }
+
+SFA_API const char* sfa_strerror(sfa_status s) {
+    switch (s) {
+        case SFA_OK: return "ok";
+        case SFA_ERR_INVALID_ARG: return "invalid argument";
+        case SFA_ERR_UNSUPPORTED: return "unsupported shape (Hq=8, Hkv=2, D=64 only)";
+        case SFA_ERR_CUDA: return "CUDA launch or runtime error";
+        case SFA_ERR_DEVICE_STATUS: return "a kernel reported a device-side error";
+    }
+    return "unknown status";
+}
+
+SFA_API unsigned long long sfa_launch_count(void) {
+    return sfa::g_launches.load(std::memory_order_relaxed);
+}
+
+SFA_API float sfa_alpha_from_theta(float theta) {
+    const double th = (double)theta;
+    return (float)(0.5 + 1.0 / (1.0 + std::exp(-th)));
+}
+
+SFA_API sfa_status sfa_alpha_schedule(sfa_schedule kind, int L, int S, const float* theta,
+                                      float* alpha_out) {
+    if (L <= 0 || !alpha_out) return SFA_ERR_INVALID_ARG;
+    switch (kind) {
+        case SFA_SCHEDULE_FIXED:
+            for (int l = 0; l < L; ++l) alpha_out[l] = 1.0f;
+            return SFA_OK;
+        case SFA_SCHEDULE_LEARNED:
+            if (!theta) return SFA_ERR_INVALID_ARG;
+            for (int l = 0; l < L; ++l) {
+                if (!std::isfinite(theta[l])) return SFA_ERR_INVALID_ARG;
+                alpha_out[l] = sfa_alpha_from_theta(theta[l]);
+            }
+            return SFA_OK;
+        case SFA_SCHEDULE_LINEAR:
+        case SFA_SCHEDULE_COPRIME: {
+            if (L < 2) return SFA_ERR_INVALID_ARG;
+            int stride = 1;
+            if (kind == SFA_SCHEDULE_COPRIME) {
+                if (S <= 0) return SFA_ERR_INVALID_ARG;
+                int a = S % L, b = L;
+                while (a) { int t = b % a; b = a; a = t; }
+                if (b != 1) return SFA_ERR_INVALID_ARG;  // gcd(S, L) must be 1
+                stride = S;
+            }
+            for (int l = 0; l < L; ++l) {
+                const long long slot = ((long long)stride * l) % L;
+                alpha_out[l] = (float)(0.5 + (double)slot / (double)(L - 1));
+            }
+            return SFA_OK;
+        }
+    }
+    return SFA_ERR_INVALID_ARG;
+}
+
+SFA_API sfa_status sfa_rung_plan(const sfa_params* p, int* n_active, int* index, int* n_floor,
+                                 float* frac, int* n_ceil) {
+    sfa_status st = validate(p);
+    if (st != SFA_OK) return st;
+    if (!n_active) return SFA_ERR_INVALID_ARG;
+    Rung r[SFA_MAX_RUNGS];
+    const int n = rung_plan(p, r);
+    *n_active = n;
+    for (int i = 0; i < n; ++i) {
+        if (index) index[i] = r[i].index;
+        if (n_floor) n_floor[i] = r[i].n;
+        if (frac) frac[i] = r[i].t;
+        if (n_ceil) n_ceil[i] = r[i].c;
+    }
+    return SFA_OK;
+}
+
+SFA_API size_t sfa_rope_table_floats(int T, int D) {
+    if (T <= 0 || D <= 0 || (D & 1)) return 0;
+    return (size_t)T * (size_t)D;
+}
+
+SFA_API sfa_status sfa_rope_table(float* table, int T, int D, float rope_theta,
+                                  cudaStream_t stream) {
+    if (!table || !aligned16(table) || T < 0 || D <= 0 || (D & 1) || T > kMaxT ||
+        !std::isfinite(rope_theta) || !(rope_theta > 0.f))
+        return SFA_ERR_INVALID_ARG;
+    if (T == 0) return SFA_OK;
+    return launched(sfa::launch_rope_table(reinterpret_cast<float2*>(table), T, D,
+                                           (double)rope_theta, stream));
+}
+
+SFA_API sfa_status sfa_forward(const sfa_params* p, const void* Q, const void* K, const void* V,
+                               const float* rope_table, void* O, float* lse,
+                               unsigned int* status, cudaStream_t stream) {
+    (void)status;
+    sfa_status st = validate(p);
+    if (st != SFA_OK) return st;
+    if (p->B == 0 || p->T == 0) return SFA_OK;
+    if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return SFA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
+    if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
+    LayerArgs a;
+    fill_args(p, &a);
+    return launched(sfa::launch_fwd_simple(a, p->dtype, Q, K, V, rope_ptr(p, rope_table), O, lse,
+                                           stream));
+}
+
+SFA_API size_t sfa_backward_workspace_size(const sfa_params* p) {
+    if (validate(p) != SFA_OK) return 0;
+    LayerArgs a;
+    fill_args(p, &a);
+    return sfa::bwd_simple_workspace(a);
+}
+
+SFA_API sfa_status sfa_backward(const sfa_params* p, const void* Q, const void* K, const void* V,
+                                const void* O, const void* dO, const float* lse,
+                                const float* rope_table, void* dQ, void* dK, void* dV,
+                                float* dalpha, float* dtheta, void* workspace,
+                                size_t workspace_bytes, unsigned int* status,
+                                cudaStream_t stream) {
+    (void)status;
+    sfa_status st = validate(p);
+    if (st != SFA_OK) return st;
+    if (!dalpha || !dtheta || (reinterpret_cast<uintptr_t>(dalpha) & 3u) ||
+        (reinterpret_cast<uintptr_t>(dtheta) & 3u))
+        return SFA_ERR_INVALID_ARG;
+    LayerArgs a;
+    fill_args(p, &a);
+    if (p->B == 0 || p->T == 0) {
+        if (cudaMemsetAsync(dalpha, 0, sizeof(float), stream) != cudaSuccess ||
+            cudaMemsetAsync(dtheta, 0, sizeof(float), stream) != cudaSuccess)
+            return launched(cudaGetLastError());
+        return SFA_OK;
+    }
+    const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
+    for (const void* q : ptrs)
+        if (!q || !aligned16(q)) return SFA_ERR_INVALID_ARG;
+    if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
+    if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
+    const size_t need = sfa::bwd_simple_workspace(a);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
+        return SFA_ERR_INVALID_ARG;
+    return launched(sfa::launch_bwd_simple(a, p->dtype, Q, K, V, O, dO, lse, rope_ptr(p, rope_table),
+                                           dQ, dK, dV, dalpha, dtheta, workspace, stream));
+}
+
+SFA_API sfa_status sfa_read_status(const unsigned int* status, unsigned int* host_word,
+                                   cudaStream_t stream) {
+    if (!status) return SFA_ERR_INVALID_ARG;
+    unsigned int w = 0;
+    if (cudaMemcpyAsync(&w, status, sizeof(w), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return SFA_ERR_CUDA;
+    }
+    if (host_word) *host_word = w;
+    return w ? SFA_ERR_DEVICE_STATUS : SFA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+// sfa_internal.cuh -- launch arguments and device helpers shared by the
+// kernels of libsfa.  Private to the CUDA library (not installed, not part of
+// the C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "sfa.h"
+
+namespace sfa {
+
+// Fixed attention shape of the paper (section 3 "Model and training"): 8 query
+// heads sharing 2 key/value heads, head dimension 64.
+constexpr int kHq = 8;
+constexpr int kHkv = 2;
+constexpr int kG = kHq / kHkv;  // query heads per key/value head
+constexpr int kD = 64;
+constexpr int kPairs = kD / 2;  // RoPE pairs (m, m + 32)
+
+// One rung as the kernels use it: the distance d = alpha * f lies strictly
+// beyond the window, floor(d) = n, t = d - n, ceil(d) = c (c = n when t = 0).
+struct Rung {
+    int n;
+    float t;
+    int c;
+    float f;    // base offset, the derivative d d / d alpha
+    int index;  // position in the caller's table
+};
+
+struct LayerArgs {
+    int B, T, W;
+    int nr;          // rungs kept (d > W and not masked for every query)
+    float scale;     // softmax scale
+    float alpha;
+    Rung r[SFA_MAX_RUNGS];
+};
+
+// Host: count of kernel launches made by the library.
+void count_launch();
+
+// Launchers (each returns the launch error, if any).
+cudaError_t launch_rope_table(float2* table, int T, int D, double theta, cudaStream_t s);
+
+cudaError_t launch_fwd_simple(const LayerArgs& a, sfa_dtype dt, const void* q, const void* k,
+                              const void* v, const float2* rope, void* o, float* lse,
+                              cudaStream_t s);
+
+size_t bwd_simple_workspace(const LayerArgs& a);
+cudaError_t launch_bwd_simple(const LayerArgs& a, sfa_dtype dt, const void* q, const void* k,
+                              const void* v, const void* o, const void* dO, const float* lse,
+                              const float2* rope, void* dq, void* dk, void* dv, float* dalpha,
+                              float* dtheta, void* ws, cudaStream_t s);
+
+// ------------------------------------------------------------ device helpers
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+constexpr unsigned kFull = 0xffffffffu;
+
+// Sum over the 32 lanes of four per-lane values (one per query head of a
+// key/value group); every lane receives all four sums.  Fixed order, so the
+// result is deterministic.
+__device__ __forceinline__ void warp_sum4(float v[4]) {
+    const int lane = threadIdx.x & 31;
+    const bool up16 = lane & 16;
+    float keep0 = up16 ? v[2] : v[0], keep1 = up16 ? v[3] : v[1];
+    const float send0 = up16 ? v[0] : v[2], send1 = up16 ? v[1] : v[3];
+    keep0 += __shfl_xor_sync(kFull, send0, 16);
+    keep1 += __shfl_xor_sync(kFull, send1, 16);
+    const bool up8 = lane & 8;
+    float keep = up8 ? keep1 : keep0;
+    const float send = up8 ? keep0 : keep1;
+    keep += __shfl_xor_sync(kFull, send, 8);
+    keep += __shfl_xor_sync(kFull, keep, 4);
+    keep += __shfl_xor_sync(kFull, keep, 2);
+    keep += __shfl_xor_sync(kFull, keep, 1);
+    v[0] = __shfl_sync(kFull, keep, 0);
+    v[1] = __shfl_sync(kFull, keep, 8);
+    v[2] = __shfl_sync(kFull, keep, 16);
+    v[3] = __shfl_sync(kFull, keep, 24);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    return x;
+}
+
+// (cos, sin) of pair m at position pos, identity without a table.
+__device__ __forceinline__ float2 rope_cs(const float2* __restrict__ rope, int pos, int m) {
+    return rope ? __ldg(rope + (size_t)pos * kPairs + m) : make_float2(1.f, 0.f);
+}
+
+}  // namespace sfa

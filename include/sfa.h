@@ -1,0 +1,193 @@
+/*
+ * sfa.h -- C ABI of libsfa, depth-staggered Fibonacci sparse attention on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the attention of "Depth-Staggered Fibonacci Spacing for
+ * Sparse Attention: Static Schedules Beat Learned Dilation and Extrapolate
+ * Where Dense Attention Fails" (arXiv 2606.28560), section 2 "Method":
+ *
+ *   For query i the attended keys are the dense window of distances 0..W
+ *   (self included) and one "rung" per base offset f_k at the continuous
+ *   distance d_k = alpha * f_k.  A rung reads key and value row i - d_k by
+ *   linear interpolation between rows i - floor(d_k) (weight 1 - t) and
+ *   i - floor(d_k) - 1 (weight t), t = d_k - floor(d_k).  RoPE is applied at
+ *   the true positions before that gather.  The offsets are shared by all
+ *   queries (a shift, not a per-position index list).  One softmax runs over
+ *   the union of window and rung entries.  The per-layer scalar is
+ *   alpha = 0.5 + sigmoid(theta) ("Per-layer scalar").
+ *
+ * Conventions fixed by this library where the paper is silent:
+ *   - d_k is the fp32 product fl32(alpha) * fl32(f_k), rounded to nearest;
+ *   - a rung with d_k <= W is dropped (its distance is in the window);
+ *   - a rung is masked for query i when i - ceil(d_k) < 0;
+ *   - RoPE pairs dimension m with m + D/2 ("rotate half"), angle
+ *     pos * rope_theta^(-2m/D);
+ *   - query head h reads key/value head h / (Hq / Hkv);
+ *   - the softmax scale defaults to 1/sqrt(D).
+ *
+ * Layouts.  Q, O, dO, dQ: [B][T][Hq][D]; K, V, dK, dV: [B][T][Hkv][D]; all
+ * row-major with D fastest, element type sfa_params.dtype.  lse: [B][T][Hq]
+ * fp32 (natural-log log-sum-exp of the scaled scores).  All tensors are
+ * device pointers aligned to 16 bytes and must not overlap one another.
+ *
+ * Ownership.  The caller allocates every buffer (outputs, workspace, RoPE
+ * table, status word).  The library allocates no device or host memory and
+ * keeps no state between calls; the rung table is copied into the kernel
+ * arguments.  Every call is asynchronous on the given stream and returns
+ * before the GPU finishes.
+ *
+ * Errors.  Invalid arguments return SFA_ERR_INVALID_ARG and shapes outside the
+ * supported set return SFA_ERR_UNSUPPORTED, both before anything is launched.
+ * A failed launch returns SFA_ERR_CUDA.  A kernel that gives up a bounded wait
+ * sets a bit in the optional device status word (see SFA_DEVSTAT_*) and
+ * returns; sfa_read_status() turns a non-zero word into SFA_ERR_DEVICE_STATUS.
+ * Outputs are undefined after any error.
+ */
+#ifndef SFA_H
+#define SFA_H
+
+#include <stddef.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SFA_API __attribute__((visibility("default")))
+#else
+#define SFA_API
+#endif
+
+#define SFA_MAX_RUNGS 32
+
+typedef enum {
+    SFA_OK = 0,
+    SFA_ERR_INVALID_ARG = 1,
+    SFA_ERR_UNSUPPORTED = 2,
+    SFA_ERR_CUDA = 3,
+    SFA_ERR_DEVICE_STATUS = 4
+} sfa_status;
+
+typedef enum { SFA_F32 = 0, SFA_BF16 = 1 } sfa_dtype;
+
+/* Bits a kernel may set in the device status word. */
+#define SFA_DEVSTAT_WAIT_TIMEOUT 0x1u  /* a bounded pipeline wait gave up */
+#define SFA_DEVSTAT_BAD_INDEX    0x2u  /* a computed row index left [0, T) */
+
+typedef struct {
+    int B, T;          /* batch, sequence length (>= 0; 0 means nothing to do) */
+    int Hq, Hkv, D;    /* heads and head dim; supported: Hq = 8, Hkv = 2, D = 64 */
+    int W;             /* window: distances 0..W (W >= 0) */
+    int K;             /* number of base offsets, 0 <= K <= SFA_MAX_RUNGS */
+    const float *rungs;/* HOST pointer to K base offsets f_k (finite, > 0) */
+    float alpha;       /* the layer's scalar (finite, > 0) */
+    float rope_theta;  /* RoPE base (1e4 in the paper); <= 0: inputs already rotated */
+    float scale;       /* softmax scale; 0 selects 1/sqrt(D) */
+    sfa_dtype dtype;   /* element type of Q, K, V, O, dO, dQ, dK, dV */
+} sfa_params;
+
+/* Library version, (major << 16) | minor. */
+SFA_API int sfa_version(void);
+
+/* Human-readable name of a status code (static string). */
+SFA_API const char *sfa_strerror(sfa_status s);
+
+/* Number of kernels this library has launched in the process so far (host
+ * counter, incremented on every successful launch). */
+SFA_API unsigned long long sfa_launch_count(void);
+
+/* ---- per-layer scalar ("Per-layer scalar", section 2) ---------------- */
+
+typedef enum {
+    SFA_SCHEDULE_FIXED = 0,   /* alpha_l = 1 */
+    SFA_SCHEDULE_LEARNED = 1, /* alpha_l = 0.5 + sigmoid(theta_l) */
+    SFA_SCHEDULE_LINEAR = 2,  /* alpha_l = 0.5 + l / (L - 1) */
+    SFA_SCHEDULE_COPRIME = 3  /* linear ramp re-assigned by l -> (S l) mod L */
+} sfa_schedule;
+
+/* alpha = 0.5 + sigmoid(theta), computed in double and rounded to float. */
+SFA_API float sfa_alpha_from_theta(float theta);
+
+/* Fills alpha_out[0..L-1] (host) with the schedule's per-layer scalars.
+ * theta (host, L values) is read only by SFA_SCHEDULE_LEARNED; S is the
+ * coprime stride (7 in the paper) and must satisfy gcd(S, L) = 1.
+ * Values are computed in double and rounded once to float. */
+SFA_API sfa_status sfa_alpha_schedule(sfa_schedule kind, int L, int S,
+                                      const float *theta, float *alpha_out);
+
+/* ---- rung preparation (host; "Attended set", section 2) -------------- */
+
+/* The rungs the kernels will use for this layer, in table order: for every
+ * base offset with d_k = fl32(alpha) * fl32(f_k) > W it reports the table
+ * index, floor(d_k), t = d_k - floor(d_k) and ceil(d_k).  Arrays are host
+ * arrays of at least p->K entries; *n_active receives the count.  This is
+ * the same routine sfa_forward and sfa_backward use. */
+SFA_API sfa_status sfa_rung_plan(const sfa_params *p, int *n_active, int *index,
+                                 int *n_floor, float *frac, int *n_ceil);
+
+/* ---- RoPE table ------------------------------------------------------ */
+
+/* Number of floats of a RoPE table for T positions and head dim D (T * D). */
+SFA_API size_t sfa_rope_table_floats(int T, int D);
+
+/* Writes the RoPE table on the device: table[pos][m] = (cos, sin) of
+ * pos * rope_theta^(-2m/D) for pos < T, m < D/2, as float pairs, angles and
+ * trigonometry in double.  The table serves every call with the same D and
+ * rope_theta and a sequence length <= T.  table: device, 16-byte aligned,
+ * sfa_rope_table_floats(T, D) floats. */
+SFA_API sfa_status sfa_rope_table(float *table, int T, int D, float rope_theta,
+                                  cudaStream_t stream);
+
+/* ---- forward ----------------------------------------------------------- */
+
+/* O = sparse attention(Q, K, V) for one layer (section 2 "Attended set").
+ *   Q [B][T][Hq][D], K and V [B][T][Hkv][D] (device, dtype p->dtype);
+ *   rope_table: from sfa_rope_table with >= T positions, p->D and
+ *     p->rope_theta; may be NULL only when p->rope_theta <= 0;
+ *   O [B][T][Hq][D] (device, dtype p->dtype), fully overwritten;
+ *   lse [B][T][Hq] fp32 (device) or NULL; required by sfa_backward;
+ *   status: device word or NULL (see SFA_DEVSTAT_*).
+ * Asynchronous on stream; one kernel launch. */
+SFA_API sfa_status sfa_forward(const sfa_params *p, const void *Q, const void *K,
+                               const void *V, const float *rope_table, void *O,
+                               float *lse, unsigned int *status, cudaStream_t stream);
+
+/* ---- backward ---------------------------------------------------------- */
+
+/* Bytes of device workspace sfa_backward needs for these parameters. */
+SFA_API size_t sfa_backward_workspace_size(const sfa_params *p);
+
+/* Gradients of a scalar loss L given dO = dL/dO (section 2 "Implementation
+ * notes": the interpolation fraction carries the gradient to alpha).
+ *   Q, K, V, O, dO: as in sfa_forward (O from sfa_forward with the same
+ *     arguments); lse: from that forward (required);
+ *   dQ [B][T][Hq][D], dK and dV [B][T][Hkv][D]: device, dtype p->dtype,
+ *     fully overwritten;
+ *   dalpha: device, 1 float, receives dL/dalpha = sum_k f_k * dL/dt_k;
+ *   dtheta: device, 1 float, receives dL/dalpha * (alpha - 0.5) * (1.5 - alpha),
+ *     the gradient to theta when alpha = 0.5 + sigmoid(theta);
+ *   workspace: device, 256-byte aligned, >= sfa_backward_workspace_size(p)
+ *     bytes, contents ignored on entry and clobbered;
+ *   status: device word or NULL.
+ * The derivative of floor/ceil and of the drop and mask decisions is zero.
+ * Asynchronous on stream; three kernel launches. */
+SFA_API sfa_status sfa_backward(const sfa_params *p, const void *Q, const void *K,
+                                const void *V, const void *O, const void *dO,
+                                const float *lse, const float *rope_table, void *dQ,
+                                void *dK, void *dV, float *dalpha, float *dtheta,
+                                void *workspace, size_t workspace_bytes,
+                                unsigned int *status, cudaStream_t stream);
+
+/* ---- device status ----------------------------------------------------- */
+
+/* Synchronises stream, copies the device status word to *host_word (may be
+ * NULL) and returns SFA_ERR_DEVICE_STATUS if it is non-zero, SFA_OK if zero. */
+SFA_API sfa_status sfa_read_status(const unsigned int *status, unsigned int *host_word,
+                                   cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFA_H */

@@ -1,0 +1,80 @@
+"""Backward parity: dQ, dK, dV, dalpha and dtheta from the CUDA path against the
+fp64 oracle on the same seeded inputs (small sizes element by element, the
+training-step workload at full size)."""
+import numpy as np
+import pytest
+import torch
+
+from fibonacci_spaced_sparse_gb300 import api, inputs, workloads
+from oracle import oracle
+from _helpers import TOL, draw, max_abs, np64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+FIB = api.FIBONACCI_BASE
+
+
+def run(B, T, dtype, *, alpha, W, rungs=FIB, layer=0, rope_theta=1e4):
+    x, f = draw(B, T, dtype, layer=layer, with_dO=True)
+    xd = to_dev(x)
+    o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], alpha=alpha, W=W, rungs=rungs,
+                             rope_theta=rope_theta)
+    dq, dk, dv, da, dth = api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse,
+                                           alpha=alpha, W=W, rungs=rungs, rope_theta=rope_theta)
+    torch.cuda.synchronize()
+    ref = oracle.backward(f["q"], f["k"], f["v"], f["dO"], W=W, rungs=rungs, alpha=alpha,
+                          rope_theta=rope_theta)
+    tol = TOL[dtype]
+    for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+        err = max_abs(np64(got), want)
+        bound = tol["grad"] * max(1.0, float(np.abs(want).max()) if want.size else 1.0)
+        assert err <= bound, (name, err, bound)
+    da_ref, dth_ref = ref[3], ref[4]
+    assert abs(float(dth.item()) - dth_ref) <= tol["dtheta"] * max(abs(dth_ref), 1e-3), (
+        float(dth.item()), dth_ref)
+    assert abs(float(da.item()) - da_ref) <= tol["dtheta"] * max(abs(da_ref), 1e-3)
+    return ref
+
+
+@pytest.mark.parametrize("alpha", [0.61, 1.0, 1.2345])
+def test_fp32_small(alpha):
+    run(2, 150, "f32", alpha=alpha, W=8, layer=2)
+
+
+@pytest.mark.parametrize("alpha,W", [(0.5, 12), (0.873, 12), (1.31, 6), (1.5, 12)])
+def test_bf16_small(alpha, W):
+    run(2, 300, "bf16", alpha=alpha, W=W, layer=3)
+
+
+def test_pow2_and_edges():
+    run(1, 257, "bf16", alpha=api.alpha_from_theta(0.4), W=10, rungs=api.pow2_base(257))
+    run(2, 1, "f32", alpha=0.7, W=12)                      # single token
+    run(2, 40, "f32", alpha=0.9, W=64)                     # dense limit
+    run(2, 40, "f32", alpha=0.9, W=5, rungs=())            # window only
+    run(2, 64, "f32", alpha=1.11, W=8, rope_theta=0.0)     # pre-rotated inputs
+
+
+def test_integer_distance_rung_at_sequence_start():
+    """alpha = 1: every t = 0; the query i = f_k uses row 0 only and the
+    t-derivative there has no row -1 (zero by convention)."""
+    run(1, 120, "f32", alpha=1.0, W=8)
+
+
+@pytest.mark.parametrize("layer", [0, 9])
+def test_train_step_full(layer):
+    wl = workloads.TRAIN_STEP
+    alphas, _ = wl.alphas()
+    run(wl.B, wl.T, "bf16", alpha=alphas[layer], W=12, layer=layer)
+
+
+def test_autograd_theta_matches_library():
+    x, _ = draw(1, 96, "f32", layer=7, with_dO=True)
+    xd = to_dev(x)
+    q, k, v = (xd[n].clone().requires_grad_(True) for n in ("q", "k", "v"))
+    theta = torch.tensor(0.31, device="cuda", requires_grad=True)
+    o = api.SparseAttention.apply(q, k, v, theta, 8)
+    (o * xd["dO"]).sum().backward()
+    alpha = api.alpha_from_theta(0.31)
+    _, _, _, _, dth_ref, _ = oracle.backward(*(x[n].double().numpy() for n in ("q", "k", "v", "dO")),
+                                              W=8, rungs=FIB, alpha=alpha)
+    assert abs(theta.grad.item() - dth_ref) <= 1e-3 * max(1.0, abs(dth_ref))

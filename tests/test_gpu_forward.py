@@ -1,0 +1,148 @@
+"""Forward parity: the CUDA path through the C ABI against the fp64 oracle on
+the same seeded inputs, element by element at sizes the oracle finishes in
+seconds, and on sampled rows at the workloads' full sizes."""
+import numpy as np
+import pytest
+import torch
+
+from fibonacci_spaced_sparse_gb300 import api, workloads
+from oracle import oracle
+from _helpers import TOL, draw, gpu_forward, max_abs, np64, sample_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+FIB = api.FIBONACCI_BASE
+
+
+def check_full(B, T, dtype, *, alpha, W, rungs, layer=0, rope_theta=1e4):
+    x, f = draw(B, T, dtype, layer=layer)
+    o, lse = gpu_forward(to_dev(x), alpha=alpha, W=W, rungs=rungs, rope_theta=rope_theta)
+    o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], W=W, rungs=rungs, alpha=alpha,
+                                    rope_theta=rope_theta)
+    eo, el = max_abs(np64(o), o_ref), max_abs(np64(lse), lse_ref)
+    assert eo <= TOL[dtype]["o"], (eo, alpha, W)
+    assert el <= TOL[dtype]["lse"], (el, alpha, W)
+    return eo
+
+
+def check_sampled(wl, layer, nrows=384):
+    alphas, _ = wl.alphas()
+    alpha, W = alphas[layer], wl.window(layer)
+    x, f = draw(wl.B, wl.T, wl.dtype, layer=layer)
+    o, lse = gpu_forward(to_dev(x), alpha=alpha, W=W, rungs=wl.rungs())
+    rows = sample_rows(wl.B, wl.T, nrows, seed=layer)
+    o_ref, lse_ref = oracle.forward_rows(f["q"], f["k"], f["v"], rows, W=W, rungs=wl.rungs(),
+                                         alpha=alpha)
+    og = np64(o)[rows[:, 0], rows[:, 1]]
+    lg = np64(lse)[rows[:, 0], rows[:, 1]]
+    assert max_abs(og, o_ref) <= TOL[wl.dtype]["o"]
+    assert max_abs(lg, lse_ref) <= TOL[wl.dtype]["lse"]
+    # properties that hold at any size: finite, rows are convex combinations
+    on = np64(o)
+    assert np.isfinite(on).all()
+    vmax = np.abs(x["v"].float().numpy()).max()
+    assert np.abs(on).max() <= vmax * (1 + 1e-2)
+
+
+# ------------------------------------------------ element-wise, small sizes --
+
+
+def test_tiny_fp32_alpha1():
+    """B=1, T=256, W=8, alpha=1, fp32: within 1e-4 of the oracle."""
+    check_full(1, 256, "f32", alpha=1.0, W=8, rungs=FIB)
+
+
+@pytest.mark.parametrize("layer", [0, 3, 7, 11, 15])
+def test_linear_stagger_small(layer):
+    alpha = api.alpha_schedule("linear", 16)[layer]
+    check_full(2, 300, "bf16", alpha=alpha, W=12, rungs=FIB, layer=layer)
+
+
+@pytest.mark.parametrize("layer", [1, 2, 9])
+def test_coprime_small(layer):
+    alpha = api.alpha_schedule("coprime", 16, 7)[layer]
+    check_full(1, 1200, "bf16", alpha=alpha, W=12, rungs=FIB, layer=layer)
+
+
+@pytest.mark.parametrize("W", [6, 8, 10, 12])
+def test_pow2_small(W):
+    alpha = api.alpha_from_theta(0.21 * W - 1.9)
+    check_full(2, 333, "bf16", alpha=alpha, W=W, rungs=api.pow2_base(333))
+
+
+@pytest.mark.parametrize("alpha", [0.5, 0.51234, 1.0, 1.37, 1.5])
+def test_fp32_fractional(alpha):
+    check_full(2, 200, "f32", alpha=alpha, W=10, rungs=FIB, layer=4)
+
+
+# ------------------------------------------------------------- edge cases --
+
+
+def test_single_token_and_first_query():
+    x, f = draw(3, 1, "bf16")
+    o, lse = gpu_forward(to_dev(x), alpha=1.0, W=12, rungs=FIB)
+    for h in range(8):
+        assert torch.equal(o[:, 0, h].cpu(), x["v"][:, 0, h // 4])
+    ref = (x["q"].double()[:, 0] * x["k"].double()[:, 0].repeat_interleave(4, 1)).sum(-1) / 8
+    assert max_abs(np64(lse[:, 0]), ref.numpy()) < 1e-4
+
+
+def test_empty_inputs_launch_nothing():
+    z = torch.empty((0, 16, 8, 64), dtype=torch.bfloat16, device="cuda")
+    zk = torch.empty((0, 16, 2, 64), dtype=torch.bfloat16, device="cuda")
+    n0 = api.launch_count()
+    o, lse = api.sfa_forward(z, zk, zk, alpha=1.0, W=12)
+    assert o.shape == z.shape and api.launch_count() == n0
+    z = torch.empty((2, 0, 8, 64), dtype=torch.bfloat16, device="cuda")
+    zk = torch.empty((2, 0, 2, 64), dtype=torch.bfloat16, device="cuda")
+    api.sfa_forward(z, zk, zk, alpha=1.0, W=12)
+    assert api.launch_count() == n0
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_window_only_and_dense_limit(dtype):
+    check_full(2, 96, dtype, alpha=0.8, W=12, rungs=())          # no rungs at all
+    check_full(2, 96, dtype, alpha=0.8, W=200, rungs=FIB)        # W >= T: causal dense
+    check_full(2, 96, dtype, alpha=1.3, W=0, rungs=FIB)          # self + rungs only
+
+
+def test_rungs_all_masked_short_sequence():
+    check_full(3, 20, "bf16", alpha=1.5, W=12, rungs=FIB)
+
+
+def test_without_rope():
+    check_full(2, 128, "f32", alpha=0.91, W=8, rungs=FIB, rope_theta=0.0)
+
+
+def test_deterministic_and_status_word():
+    x, _ = draw(2, 257, "bf16", layer=5)
+    xd = to_dev(x)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    n0 = api.launch_count()
+    o1, l1 = gpu_forward(xd, alpha=1.17, W=12, rungs=FIB, status=status)
+    o2, l2 = gpu_forward(xd, alpha=1.17, W=12, rungs=FIB, status=status)
+    assert api.launch_count() - n0 == 2          # one kernel per forward call
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    assert api.sfa_read_status(status) == 0
+
+
+# -------------------------------------------- full sizes, sampled rows --
+
+
+@pytest.mark.parametrize("layer", [0, 7, 15])
+def test_model_shape_full(layer):
+    check_sampled(workloads.MODEL_SHAPE, layer)
+
+
+@pytest.mark.parametrize("layer", [0, 5])
+def test_extrapolation_full(layer):
+    check_sampled(workloads.EXTRAPOLATION, layer)
+
+
+@pytest.mark.parametrize("layer", [0, 1, 2, 3])
+def test_pow2_full(layer):
+    check_sampled(workloads.POW2, layer)
+
+
+def test_long_forward_full():
+    check_sampled(workloads.LONG_FORWARD, 3, nrows=256)
