@@ -307,25 +307,51 @@ def run_ours(args, rank, world, local):
 
 def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
     """Same step through the C ABI from pinned host buffers: each step copies
-    every layer's Q, K, V host->device, runs the layer, and copies O back."""
+    every layer's Q, K, V host->device, runs the layer, and copies O back.
+    Copies run on their own streams so that layer l's attention overlaps the
+    upload of layer l+1 and the download of layer l-1 (double-buffered device
+    staging); events order each layer's three stages."""
     import torch
     from fibonacci_spaced_sparse_gb300 import api
     L = wl.layers
     pin = [{k: host[l][k].pin_memory() for k in ("q", "k", "v")} for l in range(L)]
     o_host = [torch.empty_like(pin[l]["q"]).pin_memory() for l in range(L)]
-    dq = [{k: torch.empty_like(pin[l][k], device=dev) for k in ("q", "k", "v")} for l in range(L)]
-    do = [torch.empty_like(dq[l]["q"]) for l in range(L)]
-    lse = [torch.empty((wl.B, wl.T, 8), dtype=torch.float32, device=dev) for _ in range(L)]
+    NB = 2
+    dq = [{k: torch.empty_like(pin[0][k], device=dev) for k in ("q", "k", "v")} for _ in range(NB)]
+    do = [torch.empty_like(dq[0]["q"]) for _ in range(NB)]
+    lse = [torch.empty((wl.B, wl.T, 8), dtype=torch.float32, device=dev) for _ in range(NB)]
     h2d = sum(pin[l][k].numel() * pin[l][k].element_size() for l in range(L) for k in pin[l])
     d2h = sum(o.numel() * o.element_size() for o in o_host)
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
 
     def step():
+        loaded = [None] * L
+        computed = [None] * L
+        freed = [None] * NB      # buffer may be overwritten once its O was downloaded
         for l in range(L):
-            for k in ("q", "k", "v"):
-                dq[l][k].copy_(pin[l][k], non_blocking=True)
-            api.sfa_forward(dq[l]["q"], dq[l]["k"], dq[l]["v"], alpha=alphas[l], W=wl.window(l),
-                            rungs=wl.rungs(), out=do[l], lse=lse[l])
-            o_host[l].copy_(do[l], non_blocking=True)
+            s = l % NB
+            with torch.cuda.stream(up):
+                if freed[s] is not None:
+                    up.wait_event(freed[s])
+                if l >= NB and computed[l - NB] is not None:
+                    up.wait_event(computed[l - NB])   # inputs of layer l-NB consumed
+                for k in ("q", "k", "v"):
+                    dq[s][k].copy_(pin[l][k], non_blocking=True)
+                loaded[l] = ev()
+                loaded[l].record(up)
+            stream.wait_event(loaded[l])
+            api.sfa_forward(dq[s]["q"], dq[s]["k"], dq[s]["v"], alpha=alphas[l], W=wl.window(l),
+                            rungs=wl.rungs(), out=do[s], lse=lse[s], stream=stream)
+            computed[l] = ev()
+            computed[l].record(stream)
+            with torch.cuda.stream(down):
+                down.wait_event(computed[l])
+                o_host[l].copy_(do[s], non_blocking=True)
+                freed[s] = ev()
+                freed[s].record(down)
+        stream.wait_stream(up)
+        stream.wait_stream(down)
 
     for _ in range(max(3, args.warmup)):
         step()

@@ -56,7 +56,9 @@ _SIGS = {
     "sfa_rung_plan": ([_PP, _IP, _IP, _IP, _FP, _IP], ctypes.c_int),
     "sfa_rope_table_floats": ([ctypes.c_int, ctypes.c_int], ctypes.c_size_t),
     "sfa_rope_table": ([_VP, ctypes.c_int, ctypes.c_int, ctypes.c_float, _VP], ctypes.c_int),
-    "sfa_forward": ([_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "sfa_forward_workspace_size": ([_PP], ctypes.c_size_t),
+    "sfa_forward": ([_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP, _VP],
+                    ctypes.c_int),
     "sfa_backward_workspace_size": ([_PP], ctypes.c_size_t),
     "sfa_backward": ([_PP] + [_VP] * 13 + [ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "sfa_read_status": ([_VP, ctypes.POINTER(ctypes.c_uint), _VP], ctypes.c_int),

@@ -143,9 +143,23 @@ def _check_qkv(q, k, v):
         raise ValueError("q, k, v must share B and T")
 
 
+_ws_cache: dict = {}
+
+
+def _workspace(device, nbytes: int) -> torch.Tensor:
+    """A per-device scratch buffer of at least nbytes (grown on demand).  Calls
+    on one device share it, so they must be ordered on one stream."""
+    key = torch.device(device)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=key)
+        _ws_cache[key] = buf
+    return buf
+
+
 def sfa_forward(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE, rope_theta: float = 1e4,
                 scale: float = 0.0, need_lse: bool = True, out=None, lse=None, status=None,
-                stream=None):
+                workspace=None, stream=None):
     """O (and LSE) of the sparse attention for one layer; see include/sfa.h."""
     _check_qkv(q, k, v)
     B, T = q.shape[0], q.shape[1]
@@ -154,10 +168,15 @@ def sfa_forward(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE, rope_the
         lse = torch.empty((B, T, 8), dtype=torch.float32, device=q.device)
     p = Params(B, T, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
                dtype=q.dtype)
+    lib = _lib.load()
+    need = int(lib.sfa_forward_workspace_size(p.ref()))
+    if workspace is None or workspace.numel() < need:
+        workspace = _workspace(q.device, need) if need else None
     tab = rope_table(T, q.device, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
-    st = _lib.load().sfa_forward(p.ref(), _vp(q), _vp(k), _vp(v), _vp(tab), _vp(o),
-                                 _vp(lse if need_lse else None), _vp(status),
-                                 _stream(q.device, stream))
+    st = lib.sfa_forward(p.ref(), _vp(q), _vp(k), _vp(v), _vp(tab), _vp(o),
+                         _vp(lse if need_lse else None), _vp(workspace),
+                         ctypes.c_size_t(workspace.numel() if workspace is not None else 0),
+                         _vp(status), _stream(q.device, stream))
     _lib.check(st, "sfa_forward")
     return o, (lse if need_lse else None)
 

@@ -8,6 +8,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "sfa.h"
@@ -48,7 +49,8 @@ sfa_status validate(const sfa_params* p) {
 
 // Rung preparation ("Attended set"): d = fl32(alpha) * fl32(f) rounded to
 // nearest; rungs with d <= W are dropped (inside the window); rungs whose
-// ceil(d) exceeds T - 1 are masked for every query and are left out too.
+// ceil(d) exceeds T - 1 are masked for every query and are left out too.  The
+// kept rungs are ordered by increasing distance.
 int rung_plan(const sfa_params* p, Rung* out) {
     int n = 0;
     for (int k = 0; k < p->K; ++k) {
@@ -65,7 +67,14 @@ int rung_plan(const sfa_params* p, Rung* out) {
         r.c = (int)ce;
         r.f = p->rungs[k];
         r.index = k;
-        out[n++] = r;
+        // insertion by increasing distance (stable): the rungs a query tile can
+        // use are then a prefix of the list
+        int pos = n++;
+        while (pos > 0 && (out[pos - 1].n > r.n || (out[pos - 1].n == r.n && out[pos - 1].t > r.t))) {
+            out[pos] = out[pos - 1];
+            --pos;
+        }
+        out[pos] = r;
     }
     return n;
 }
@@ -82,6 +91,18 @@ void fill_args(const sfa_params* p, LayerArgs* a) {
 
 const float2* rope_ptr(const sfa_params* p, const float* table) {
     return p->rope_theta > 0.f ? reinterpret_cast<const float2*>(table) : nullptr;
+}
+
+// The bf16 forward runs on the tensor-core kernel; fp32, and windows wider
+// than that kernel takes, run on the fp32-arithmetic kernel.
+// SFA_FORWARD_KERNEL=simple in the environment selects the fp32-arithmetic
+// kernel for bf16 too (read once), to compare the two on the same inputs.
+bool use_mma(const sfa_params* p, const LayerArgs& a) {
+    static const bool force_simple = [] {
+        const char* e = std::getenv("SFA_FORWARD_KERNEL");
+        return e && std::strcmp(e, "simple") == 0;
+    }();
+    return p->dtype == SFA_BF16 && sfa::fwd_mma_supported(a) && !force_simple;
 }
 
 sfa_status launched(cudaError_t e) {
@@ -185,10 +206,16 @@ SFA_API sfa_status sfa_rope_table(float* table, int T, int D, float rope_theta,
                                            (double)rope_theta, stream));
 }
 
+SFA_API size_t sfa_forward_workspace_size(const sfa_params* p) {
+    if (validate(p) != SFA_OK) return 0;
+    LayerArgs a;
+    fill_args(p, &a);
+    return use_mma(p, a) ? sfa::fwd_mma_workspace(a, p->rope_theta > 0.f) : 0;
+}
+
 SFA_API sfa_status sfa_forward(const sfa_params* p, const void* Q, const void* K, const void* V,
-                               const float* rope_table, void* O, float* lse,
-                               unsigned int* status, cudaStream_t stream) {
-    (void)status;
+                               const float* rope_table, void* O, float* lse, void* workspace,
+                               size_t workspace_bytes, unsigned int* status, cudaStream_t stream) {
     sfa_status st = validate(p);
     if (st != SFA_OK) return st;
     if (p->B == 0 || p->T == 0) return SFA_OK;
@@ -198,6 +225,14 @@ SFA_API sfa_status sfa_forward(const sfa_params* p, const void* Q, const void* K
     if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
     LayerArgs a;
     fill_args(p, &a);
+    if (use_mma(p, a)) {
+        const size_t need = sfa::fwd_mma_workspace(a, p->rope_theta > 0.f);
+        if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
+                     workspace_bytes < need))
+            return SFA_ERR_INVALID_ARG;
+        return launched(sfa::launch_fwd_mma(a, Q, K, V, rope_ptr(p, rope_table), O, lse, workspace,
+                                            status, stream));
+    }
     return launched(sfa::launch_fwd_simple(a, p->dtype, Q, K, V, rope_ptr(p, rope_table), O, lse,
                                            stream));
 }

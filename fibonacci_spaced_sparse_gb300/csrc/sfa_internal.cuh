@@ -33,7 +33,7 @@ struct Rung {
 
 struct LayerArgs {
     int B, T, W;
-    int nr;          // rungs kept (d > W and not masked for every query)
+    int nr;          // rungs kept (d > W and not masked for every query), by increasing d
     float scale;     // softmax scale
     float alpha;
     Rung r[SFA_MAX_RUNGS];
@@ -48,6 +48,12 @@ cudaError_t launch_rope_table(float2* table, int T, int D, double theta, cudaStr
 cudaError_t launch_fwd_simple(const LayerArgs& a, sfa_dtype dt, const void* q, const void* k,
                               const void* v, const float2* rope, void* o, float* lse,
                               cudaStream_t s);
+
+bool fwd_mma_supported(const LayerArgs& a);
+size_t fwd_mma_workspace(const LayerArgs& a, bool rope);
+cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, const void* v,
+                           const float2* rope, void* o, float* lse, void* ws, unsigned* status,
+                           cudaStream_t s);
 
 size_t bwd_simple_workspace(const LayerArgs& a);
 cudaError_t launch_bwd_simple(const LayerArgs& a, sfa_dtype dt, const void* q, const void* k,

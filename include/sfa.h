@@ -118,11 +118,12 @@ SFA_API sfa_status sfa_alpha_schedule(sfa_schedule kind, int L, int S,
 
 /* ---- rung preparation (host; "Attended set", section 2) -------------- */
 
-/* The rungs the kernels will use for this layer, in table order: for every
- * base offset with d_k = fl32(alpha) * fl32(f_k) > W it reports the table
- * index, floor(d_k), t = d_k - floor(d_k) and ceil(d_k).  Arrays are host
- * arrays of at least p->K entries; *n_active receives the count.  This is
- * the same routine sfa_forward and sfa_backward use. */
+/* The rungs the kernels will use for this layer, by increasing distance: for
+ * every base offset with d_k = fl32(alpha) * fl32(f_k) > W and
+ * ceil(d_k) <= T - 1 (rungs beyond that are masked for every query) it
+ * reports the table index, floor(d_k), t = d_k - floor(d_k) and ceil(d_k).
+ * Arrays are host arrays of at least p->K entries; *n_active receives the
+ * count.  This is the same routine sfa_forward and sfa_backward use. */
 SFA_API sfa_status sfa_rung_plan(const sfa_params *p, int *n_active, int *index,
                                  int *n_floor, float *frac, int *n_ceil);
 
@@ -141,17 +142,26 @@ SFA_API sfa_status sfa_rope_table(float *table, int T, int D, float rope_theta,
 
 /* ---- forward ----------------------------------------------------------- */
 
+/* Bytes of device workspace sfa_forward needs (0 when it needs none).  The
+ * bf16 path keeps the rotated keys there: B * T * Hkv * D * 2 bytes. */
+SFA_API size_t sfa_forward_workspace_size(const sfa_params *p);
+
 /* O = sparse attention(Q, K, V) for one layer (section 2 "Attended set").
  *   Q [B][T][Hq][D], K and V [B][T][Hkv][D] (device, dtype p->dtype);
  *   rope_table: from sfa_rope_table with >= T positions, p->D and
  *     p->rope_theta; may be NULL only when p->rope_theta <= 0;
  *   O [B][T][Hq][D] (device, dtype p->dtype), fully overwritten;
  *   lse [B][T][Hq] fp32 (device) or NULL; required by sfa_backward;
+ *   workspace: device, 256-byte aligned, >= sfa_forward_workspace_size(p)
+ *     bytes (may be NULL when that size is 0), clobbered;
  *   status: device word or NULL (see SFA_DEVSTAT_*).
- * Asynchronous on stream; one kernel launch. */
+ * bf16: RoPE on the keys (one launch, skipped when rope_theta <= 0), then the
+ * tensor-core attention kernel (one launch), for W <= 30; fp32 and wider
+ * windows: one fp32-arithmetic kernel.  Asynchronous on stream. */
 SFA_API sfa_status sfa_forward(const sfa_params *p, const void *Q, const void *K,
                                const void *V, const float *rope_table, void *O,
-                               float *lse, unsigned int *status, cudaStream_t stream);
+                               float *lse, void *workspace, size_t workspace_bytes,
+                               unsigned int *status, cudaStream_t stream);
 
 /* ---- backward ---------------------------------------------------------- */
 

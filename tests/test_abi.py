@@ -127,7 +127,8 @@ def _params(**kw):
 def test_validation_codes(lib):
     fake = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails validation
     null = ctypes.c_void_p(0)
-    fwd = lambda p, q=fake, o=fake, tab=fake: lib.sfa_forward(p.ref(), q, fake, fake, tab, o, null, null, null)
+    fwd = lambda p, q=fake, o=fake, tab=fake: lib.sfa_forward(p.ref(), q, fake, fake, tab, o, null,
+                                                              fake, 1 << 40, null, null)
     assert fwd(_params(Hq=4)) == _lib.SFA_ERR_UNSUPPORTED
     assert fwd(_params(D=128)) == _lib.SFA_ERR_UNSUPPORTED
     assert fwd(_params(W=-1)) == _lib.SFA_ERR_INVALID_ARG
@@ -141,7 +142,19 @@ def test_validation_codes(lib):
     assert fwd(_params(), tab=null) == _lib.SFA_ERR_INVALID_ARG    # rope on, no table
     p = _params(T=1 << 25)
     assert fwd(p) == _lib.SFA_ERR_UNSUPPORTED
-    assert lib.sfa_forward(None, fake, fake, fake, fake, fake, null, null, null) == _lib.SFA_ERR_INVALID_ARG
+    assert lib.sfa_forward(None, fake, fake, fake, fake, fake, null, fake, 0, null,
+                           null) == _lib.SFA_ERR_INVALID_ARG
+    # bf16 needs the rotated-key workspace: too small or misaligned is rejected
+    p = _params()
+    need = lib.sfa_forward_workspace_size(p.ref())
+    assert need == 2 * 64 * 2 * 64 * 2
+    ws_call = lambda ws, n: lib.sfa_forward(p.ref(), fake, fake, fake, fake, fake, null, ws, n,
+                                            null, null)
+    assert ws_call(fake, need - 1) == _lib.SFA_ERR_INVALID_ARG
+    assert ws_call(ctypes.c_void_p(0x10010), need) == _lib.SFA_ERR_INVALID_ARG
+    assert ws_call(null, need) == _lib.SFA_ERR_INVALID_ARG
+    assert lib.sfa_forward_workspace_size(_params(dtype=__import__("torch").float32).ref()) == 0
+    assert lib.sfa_forward_workspace_size(_params(rope_theta=0.0).ref()) == 0
     # nothing to do: B = 0 returns before looking at the pointers
     assert fwd(_params(B=0), q=null, o=null, tab=null) == _lib.SFA_OK
     # backward: workspace too small, missing lse
