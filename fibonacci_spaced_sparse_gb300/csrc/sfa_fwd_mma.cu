@@ -11,28 +11,36 @@
 //  1. rope_k_kernel: Khat = RoPE(K) at the true positions, bf16, into the
 //     caller's workspace (every key row is rotated once, then re-read from L2
 //     by every tile that needs it).
-//  2. fwd_mma_kernel, persistent, (1 producer + 8 consumer) warps per CTA.
-//     A CTA owns a tile of TQ = 32 consecutive queries of one sequence b and
-//     one key/value head g (4 query heads).  The producer warp streams, with
-//     cp.async (zero fill before the sequence start and past its end), the
-//     window block (rows i0 - W .. i0 + TQ - 1) and, per rung k, the block of
-//     rows i0 - n_k - 1 .. i0 + TQ - 1 - n_k of Khat and V into an mbarrier
-//     ring of shared-memory slots.  Each consumer warp owns two query pairs.
-//     For a pair (i, i + 1) the scores are formed "keys on M": S^T = Khat_rows
-//     (16 x 64) . Qhat^T (64 x 8), N = 2 queries x 4 heads.  Five rungs share
-//     one 16-row M tile (rows i - n - 1, i - n, i - n + 1 per rung); the lerp
-//     acts on the scores, s = (1 - t) s(row i - n) + t s(row i - n - 1), which
-//     equals the score of the interpolated key by linearity, and the
-//     probability p is split back onto the two rows as p (1 - t) and p t, so
-//     P^T V_rows forms the interpolated value.  One online softmax (base 2,
-//     lazy rescale: the running max is raised only when a score exceeds it by
-//     more than 2^8) runs over window and rung entries; O^T accumulates in
-//     registers and is transposed with movmatrix on the way out.
+//  2. fwd_mma_kernel, persistent, (1 producer + 7 consumer) warps per CTA.
+//     A CTA owns a tile of TQ = 28 consecutive queries of one sequence b and
+//     one key/value head g (4 query heads).  The producer (one lane) loads,
+//     with tiled TMA boxes, the window block (rows i0 - W .. i0 + TQ - 1) and,
+//     per rung k, the block of rows i0 - n_k - 1 .. i0 + TQ - 1 - n_k of Khat
+//     and V into an mbarrier ring of shared-memory slots (rows outside the
+//     sequence arrive as zeros), plus the RoPE rows of the tile's queries.
+//     Each consumer warp owns two query pairs.  For a pair (i, i + 1) the
+//     scores are formed "keys on M": S^T = Khat_rows (16 x 64) . Qhat^T
+//     (64 x 8), N = 2 queries x 4 heads.  Five rungs share one 16-row M tile
+//     (rows i - n - 1, i - n, i - n + 1 per rung); the lerp acts on the
+//     scores, s = (1 - t) s(row i - n) + t s(row i - n - 1), which equals the
+//     score of the interpolated key by linearity, and the probability p is
+//     split back onto the two rows as p (1 - t) and p t, so P^T V_rows forms
+//     the interpolated value.  One online softmax (base 2, lazy rescale: the
+//     running max is raised only when a score exceeds it by more than 2^8)
+//     runs over window and rung entries; O^T accumulates in registers and is
+//     transposed with movmatrix on the way out.
 //
-// Shared-memory rows are 128 bytes (64 bf16).  Chunk c (16 bytes) of slot row
-// r lives at chunk c ^ ((r + phase) & 7); each rung of an M tile gets phase
-// 3 x (its position in the tile) so the 8 rows of every ldmatrix land in 8
-// different bank groups.
+// Shared memory: each tensor region of a slot is 1024-byte aligned and filled
+// by TMA with the 128-byte swizzle (16-byte chunk c of region row r stored at
+// chunk c ^ (r & 7)).  The box of rung position p of an M tile starts
+// (3p mod 8) rows early, so the rows the consumers read from different rungs
+// of one tile fall in different swizzle phases and every ldmatrix (8 rows)
+// touches 8 different bank groups.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
 #include "sfa_internal.cuh"
 #include "sfa_mma.cuh"
 
@@ -40,25 +48,35 @@ namespace sfa {
 
 namespace {
 
+using namespace mma;
+
 constexpr int TQ = 28;                 // queries per tile
 constexpr int NCW = 7;                 // consumer warps (2 query pairs each)
 constexpr int NTHREADS = (NCW + 1) * 32;
-constexpr int NRS = 8;                 // rung slots
+constexpr int NRS = 7;                 // rung slots
 constexpr int NWS = 2;                 // window slots
-constexpr int RUNG_ROWS = TQ + 1;
+constexpr int MAXPH = 7;               // largest box offset of a rung position
+constexpr int RUNG_ROWS = TQ + 1;      // rows a rung block needs
+constexpr int RUNG_BOX = RUNG_ROWS + MAXPH;
 constexpr int ROWB = 128;              // bytes of one 64-element bf16 row
-constexpr int PITCH = 144;             // shared-memory row pitch (128 + 16)
 constexpr int TABB = kPairs * 8;       // bytes of one RoPE table row (32 x (cos, sin))
 constexpr int RUNGS_PER_TILE = 5;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.0f;          // raise the running max past this margin
 
+constexpr unsigned round1k(unsigned x) { return (x + 1023u) & ~1023u; }
+constexpr unsigned kRungRegion = round1k(RUNG_BOX * ROWB);  // one tensor of a rung slot
+constexpr unsigned kRungSlotBytes = 2 * kRungRegion;        // Khat region, then V region
+constexpr unsigned kHeaderBytes = 1024;                     // barriers, flag, rung table
+
 struct FwdParams {
+    CUtensorMap kmap_w;      // Khat, box of win_rows rows
+    CUtensorMap vmap_w;      // V, box of win_rows rows
+    CUtensorMap kmap_r[5];   // Khat, box of RUNG_ROWS + rung_phase(p) rows, rung position p
+    CUtensorMap vmap_r[5];   // V, same boxes
     LayerArgs a;
     const __nv_bfloat16* q;
-    const __nv_bfloat16* khat;
-    const __nv_bfloat16* v;
     const float2* rope;      // nullptr: Q is used as given
     __nv_bfloat16* o;
     float* lse;
@@ -66,16 +84,12 @@ struct FwdParams {
     int ntq;                 // query tiles per sequence
     int ntiles;              // B * ntq * Hkv
     int win_rows;            // TQ + W
-    int nwt;                 // window M tiles (1 or 2)
-    unsigned win_slot_bytes; // Khat + V rows and the tile's RoPE rows
+    int nwt;                 // window M tiles of a query quad (W + 4 rows)
+    unsigned win_region;     // bytes of one tensor region of a window slot
+    unsigned win_slot_bytes; // Khat + V regions and the tile's RoPE rows
 };
 
-using namespace mma;
-
-// Rung position p of an M tile stores its rows 16 (3p mod 8) bytes into its
-// slot; with the 144-byte pitch, chunk c of row r then sits in bank group
-// (3p + r + c) mod 8, so the 8 rows of every ldmatrix hit 8 bank groups.
-__device__ __forceinline__ uint32_t phase_off(int p) { return (uint32_t)(((3 * p) & 7) << 4); }
+__device__ __forceinline__ int rung_phase(int p) { return (3 * p) & 7; }
 
 // -------------------------------------------------------------- tile map
 
@@ -92,20 +106,21 @@ __device__ __forceinline__ Tile decode(const FwdParams& P, int t) {
     return x;
 }
 
-// Rungs are sorted by ceil(d): those usable by some query of the tile form a prefix.
-__device__ __forceinline__ int active_rungs(const LayerArgs& a, int i0) {
-    int n = 0;
-    while (n < a.nr && a.r[n].c <= i0 + TQ - 1) ++n;
-    return n;
-}
-
 // ---------------------------------------------------------- smem layout
+
+struct SRung {
+    int n;
+    float t;
+    int c;
+};
 
 struct Smem {
     uint32_t bars;      // full_w[NWS], empty_w[NWS], full_r[NRS], empty_r[NRS]
     uint32_t win;       // NWS window slots
     uint32_t rung;      // NRS rung slots
     int* abort_flag;
+    int* kt;            // per window slot: rungs usable by the slot's tile
+    const SRung* r;     // the kept rungs, by increasing distance
 };
 
 __device__ __forceinline__ uint32_t bar_full_w(const Smem& s, int i) { return s.bars + 8 * i; }
@@ -115,88 +130,68 @@ __device__ __forceinline__ uint32_t bar_empty_r(const Smem& s, int i) {
     return s.bars + 8 * (2 * NWS + NRS + i);
 }
 constexpr int kBarBytes = 8 * 2 * (NWS + NRS);
-constexpr int kHeaderBytes = 256;  // barriers + abort flag, 128-aligned slots follow
-// Khat rows then V rows at PITCH, after the rung's phase offset (<= 112 bytes)
-constexpr unsigned kRungSlotBytes = ((2u * RUNG_ROWS * PITCH + 112u) + 127u) & ~127u;
+constexpr int kFlagOffset = kBarBytes;
+constexpr int kKtOffset = kFlagOffset + 4;   // per window slot: rungs usable by its tile
+constexpr int kRungTableOffset = 256;
+static_assert(kKtOffset + 4 * NWS <= kRungTableOffset, "header overflow");
+static_assert(kRungTableOffset + SFA_MAX_RUNGS * 12 <= (int)kHeaderBytes, "header overflow");
+
+// Rungs are sorted by ceil(d): those usable by some query of the tile form a prefix.
+__device__ __forceinline__ int active_rungs(const Smem& S, int nr, int i0) {
+    int n = 0;
+    while (n < nr && S.r[n].c <= i0 + TQ - 1) ++n;
+    return n;
+}
 
 // ------------------------------------------------------------ producer
 
-// Rows row0 .. row0 + rows - 1 of Khat and V (head g of sequence b) into a
-// slot at `dst` (Khat rows, then V rows, PITCH apart): one bulk copy per valid
-// row, rows outside [0, T) zero filled by the warp.  Lane 0 announces the
-// bytes on the full barrier first.
-__device__ __forceinline__ void stage_rows(const FwdParams& P, uint32_t dst, int rows, int b, int g,
-                                           int row0, uint32_t bar, uint32_t extra_bytes, int lane) {
-    const int T = P.a.T;
-    const int lo = min(rows, max(0, -row0));                 // valid rows [lo, hi)
-    const int hi = max(lo, min(rows, T - row0));
-    // zero rows outside the sequence: 8 stores of 16 bytes per row and tensor
-    const int nzero = rows - max(0, hi - lo);
-    for (int z = lane; z < nzero * 16; z += 32) {
-        const int zr = z >> 4, part = z & 15;
-        const int r = zr < lo ? zr : hi + (zr - lo);
-        const int tensor = part >> 3, chunk = part & 7;
-        st_zero16(dst + (uint32_t)((tensor * rows + r) * PITCH + chunk * 16));
-    }
-    __syncwarp();
-    const uint32_t bytes = (uint32_t)max(0, hi - lo) * 2u * ROWB + extra_bytes;
-    if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-    __syncwarp();
-    for (int e = lane; e < 2 * max(0, hi - lo); e += 32) {
-        const int tensor = e & 1;
-        const int r = lo + (e >> 1);
-        const size_t off = (((size_t)b * T + row0 + r) * kHkv + g) * kD;
-        bulk_g2s(dst + (uint32_t)((tensor * rows + r) * PITCH), (tensor ? P.v : P.khat) + off, ROWB, bar);
-    }
-}
-
-__device__ void producer(const FwdParams& P, const Smem& S, int lane) {
+__device__ void producer(const FwdParams& P, const Smem& S) {
     int wcount = 0, rcount = 0;
     for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
         const Tile x = decode(P, t);
         {
             const int slot = wcount % NWS;
-            const uint32_t par = ((wcount / NWS) & 1) ^ 1;
-            bool ok = mbar_wait(bar_empty_w(S, slot), par, S.abort_flag);
-            if (!__all_sync(kFull, ok)) goto fail;
+            if (!mbar_wait(bar_empty_w(S, slot), ((wcount / NWS) & 1) ^ 1, S.abort_flag)) goto fail;
             const uint32_t base = S.win + slot * P.win_slot_bytes;
-            // RoPE rows of the tile's query positions (read by the consumers' Q rotation)
+            const uint32_t full = bar_full_w(S, slot);
             const int nq = min(TQ, P.a.T - x.i0);
             const uint32_t tab_bytes = P.rope ? (uint32_t)nq * TABB : 0u;
-            stage_rows(P, base, P.win_rows, x.b, x.g, x.i0 - P.a.W, bar_full_w(S, slot), tab_bytes,
-                       lane);
-            if (P.rope && lane == 0)
-                bulk_g2s(base + (uint32_t)(2 * P.win_rows * PITCH), P.rope + (size_t)x.i0 * kPairs,
-                         tab_bytes, bar_full_w(S, slot));
+            S.kt[slot] = active_rungs(S, P.a.nr, x.i0);  // published by the arrive below
+            mbar_arrive_expect_tx(full, 2u * P.win_rows * ROWB + tab_bytes);
+            tma_load_4d(base, &P.kmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
+            tma_load_4d(base + P.win_region, &P.vmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
+            // RoPE rows of the tile's query positions (read by the consumers' Q rotation)
+            if (P.rope)
+                bulk_g2s(base + 2 * P.win_region, P.rope + (size_t)x.i0 * kPairs, tab_bytes, full);
             ++wcount;
         }
         {
-            const int kt = active_rungs(P.a, x.i0);
+            const int kt = S.kt[(wcount - 1) % NWS];
             for (int k = 0; k < kt; ++k) {
                 const int slot = rcount % NRS;
-                const uint32_t par = ((rcount / NRS) & 1) ^ 1;
-                bool ok = mbar_wait(bar_empty_r(S, slot), par, S.abort_flag);
-                if (!__all_sync(kFull, ok)) goto fail;
-                stage_rows(P, S.rung + slot * kRungSlotBytes + phase_off(k % RUNGS_PER_TILE), RUNG_ROWS,
-                           x.b, x.g, x.i0 - P.a.r[k].n - 1, bar_full_r(S, slot), 0u, lane);
+                if (!mbar_wait(bar_empty_r(S, slot), ((rcount / NRS) & 1) ^ 1, S.abort_flag)) goto fail;
+                const uint32_t base = S.rung + slot * kRungSlotBytes;
+                const uint32_t full = bar_full_r(S, slot);
+                const int pos = k % RUNGS_PER_TILE;
+                const int ph = rung_phase(pos);
+                const int row0 = x.i0 - S.r[k].n - 1 - ph;
+                mbar_arrive_expect_tx(full, 2u * (RUNG_ROWS + ph) * ROWB);
+                tma_load_4d(base, &P.kmap_r[pos], 0, x.g, row0, x.b, full);
+                tma_load_4d(base + kRungRegion, &P.vmap_r[pos], 0, x.g, row0, x.b, full);
                 ++rcount;
             }
         }
     }
     return;
 fail:
-    if (lane == 0) {
-        *S.abort_flag = 1;
-        if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
-    }
+    *S.abort_flag = 1;
+    if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
     // no copy of this CTA may land after it exits: wait (bounded) for every
     // slot's last announced phase
-    if (lane == 0) {
-        for (int n = max(0, wcount - NWS); n < wcount; ++n)
-            (void)mbar_wait(bar_full_w(S, n % NWS), (n / NWS) & 1, nullptr);
-        for (int n = max(0, rcount - NRS); n < rcount; ++n)
-            (void)mbar_wait(bar_full_r(S, n % NRS), (n / NRS) & 1, nullptr);
-    }
+    for (int n = max(0, wcount - NWS); n < wcount; ++n)
+        (void)mbar_wait(bar_full_w(S, n % NWS), (n / NWS) & 1, nullptr);
+    for (int n = max(0, rcount - NRS); n < rcount; ++n)
+        (void)mbar_wait(bar_full_r(S, n % NRS), (n / NRS) & 1, nullptr);
 }
 
 // ------------------------------------------------------------ consumers
@@ -269,155 +264,274 @@ __device__ __forceinline__ void start_unit(const FwdParams& P, uint32_t tab, int
     U.l[0] = U.l[1] = 0.f;
 }
 
-// S^T (16 rows x 8 columns) = Khat rows . Qhat^T; `kaddr` is this lane's
-// ldmatrix row (row (lane & 7) + 8 ((lane >> 3) & 1) of the tile).
-__device__ __forceinline__ void scores(uint32_t kaddr, const Unit& U, float c[4]) {
-    c[0] = c[1] = c[2] = c[3] = 0.f;
-    const uint32_t hi = (uint32_t)(((threadIdx.x & 31) >> 4) << 4);
+// Per-thread constants of the M-tile layouts (independent of the tile).
+struct Lane {
+    int g8, tig, q;   // fragment row group, column pair, query of this thread's C columns
+    int rk, rv;       // M row this lane feeds to ldmatrix: Khat (A) and V (A, .trans)
+    int pk, pv;       // rung position of those rows in a rung tile (5: the pad row)
+    int ok, ov;       // their region-row offset from u (e + phase; unused for the pad row)
+    int p_lo, p_hi;   // rung position of this thread's C rows g8 and g8 + 8
+    bool b_lo, b_hi;  // the row is row b of query q's interpolation (e == q, not the pad)
+    unsigned wmask;   // window: bit (8 wt + 4 k + e) set when M row 16 wt + g8 + 8 (e/2)
+                      // is a window distance of quad query 2k + q (before the start check)
+};
+
+__device__ __forceinline__ Lane make_lane(int lane, int W) {
+    Lane L;
+    L.g8 = lane >> 2;
+    L.tig = lane & 3;
+    L.q = L.tig >> 1;
+    L.rk = (lane & 7) + (((lane >> 3) & 1) << 3);
+    L.rv = (lane & 7) + ((lane >> 4) << 3);
+    L.pk = L.rk < 15 ? L.rk / 3 : 5;
+    L.pv = L.rv < 15 ? L.rv / 3 : 5;
+    L.ok = L.rk < 15 ? L.rk - 3 * L.pk + rung_phase(L.pk) : 7;
+    L.ov = L.rv < 15 ? L.rv - 3 * L.pv + rung_phase(L.pv) : 7;
+    const int rlo = L.g8, rhi = L.g8 + 8;
+    L.p_lo = rlo / 3;
+    L.p_hi = rhi < 15 ? rhi / 3 : 5;
+    L.b_lo = (rlo - 3 * L.p_lo) == L.q;
+    L.b_hi = rhi < 15 && (rhi - 3 * L.p_hi) == L.q;
+    L.wmask = 0u;
+    for (int wt = 0; wt < 3; ++wt)
+        for (int k = 0; k < 2; ++k)
+            for (int e = 0; e < 4; ++e) {
+                const int R = 16 * wt + L.g8 + ((e >> 1) << 3);
+                const int qq = 2 * k + L.q;
+                if (R >= qq && R <= W + qq) L.wmask |= 1u << (8 * wt + 4 * k + e);
+            }
+    return L;
+}
+
+// S^T (16 rows x 8 columns) = Khat rows . Qhat^T for the units in U[0..NU).
+// This lane feeds ldmatrix row L.rk of the tile: region row r at `row`.
+template <int NU>
+__device__ __forceinline__ void scores(uint32_t row, int r, const Unit* U, float c[][4]) {
+#pragma unroll
+    for (int k = 0; k < NU; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = 0.f;
+    const int hi = (threadIdx.x & 31) >> 4;
+    const int x = r & 7;
 #pragma unroll
     for (int s = 0; s < 4; ++s) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4(kaddr + 32 * s + hi, a0, a1, a2, a3);
-        mma16816(c, a0, a1, a2, a3, U.qf[s][0], U.qf[s][1]);
+        ldsm_x4(row + (uint32_t)((((2 * s + hi) ^ x) & 7) << 4), a0, a1, a2, a3);
+#pragma unroll
+        for (int k = 0; k < NU; ++k) mma16816(c[k], a0, a1, a2, a3, U[k].qf[s][0], U[k].qf[s][1]);
     }
 }
 
-// O^T += V_rows^T . P^T, P^T given as bf16 B fragments b0 (rows 0-7), b1
-// (rows 8-15); `vaddr` is this lane's ldmatrix row (row (lane & 7) + 8 (lane >> 4)).
-__device__ __forceinline__ void accumulate(uint32_t vaddr, uint32_t b0, uint32_t b1, Unit& U) {
-    const uint32_t hi = (uint32_t)((((threadIdx.x & 31) >> 3) & 1) << 4);
+// O^T += V_rows^T . P^T for the units in U[0..NU), P^T given as bf16 B
+// fragments b[k][0] (rows 0-7), b[k][1] (rows 8-15).  This lane feeds
+// ldmatrix row L.rv.
+template <int NU>
+__device__ __forceinline__ void accumulate(uint32_t row, int r, const uint32_t b[][2], Unit* U) {
+    const int hi = ((threadIdx.x & 31) >> 3) & 1;
+    const int x = r & 7;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(vaddr + 32 * j + hi, a0, a1, a2, a3);
-        mma16816(U.o[j], a0, a1, a2, a3, b0, b1);
+        ldsm_x4_t(row + (uint32_t)((((2 * j + hi) ^ x) & 7) << 4), a0, a1, a2, a3);
+#pragma unroll
+        for (int k = 0; k < NU; ++k) mma16816(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
     }
 }
 
-// Online-softmax step for this thread's 4 candidate scores (rows lo/hi x 2
-// columns, -inf where absent): raises the running max lazily, returns the
-// probabilities in p.
-__device__ __forceinline__ void softmax_step(Unit& U, const float s[4], float p[4]) {
+// Raise the running max of this thread's two columns to the column max of s
+// (reduced over the 8 threads holding the column) and rescale O^T and l.
+__device__ __forceinline__ void raise_max(Unit& U, const float s[4]) {
     float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
     for (int w = 4; w <= 16; w <<= 1) {
         mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, w));
         mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, w));
     }
-    const bool need = (mx0 > U.m[0] + kLazy) || (mx1 > U.m[1] + kLazy);
-    if (__any_sync(kFull, need)) {
-        const float n0 = fmaxf(U.m[0], mx0), n1 = fmaxf(U.m[1], mx1);
-        const float c0 = (U.m[0] == -INFINITY) ? (n0 == -INFINITY ? 1.f : 0.f) : fast_exp2(U.m[0] - n0);
-        const float c1 = (U.m[1] == -INFINITY) ? (n1 == -INFINITY ? 1.f : 0.f) : fast_exp2(U.m[1] - n1);
-        U.m[0] = n0;
-        U.m[1] = n1;
-        U.l[0] *= c0;
-        U.l[1] *= c1;
+    const float n0 = fmaxf(U.m[0], mx0), n1 = fmaxf(U.m[1], mx1);
+    const float c0 = (U.m[0] == -INFINITY) ? (n0 == -INFINITY ? 1.f : 0.f) : fast_exp2(U.m[0] - n0);
+    const float c1 = (U.m[1] == -INFINITY) ? (n1 == -INFINITY ? 1.f : 0.f) : fast_exp2(U.m[1] - n1);
+    U.m[0] = n0;
+    U.m[1] = n1;
+    U.l[0] *= c0;
+    U.l[1] *= c1;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            U.o[j][0] *= c0;
-            U.o[j][2] *= c0;
-            U.o[j][1] *= c1;
-            U.o[j][3] *= c1;
-        }
+    for (int j = 0; j < 4; ++j) {
+        U.o[j][0] *= c0;
+        U.o[j][2] *= c0;
+        U.o[j][1] *= c1;
+        U.o[j][3] *= c1;
     }
-    p[0] = s[0] == -INFINITY ? 0.f : fast_exp2(s[0] - U.m[0]);
-    p[1] = s[1] == -INFINITY ? 0.f : fast_exp2(s[1] - U.m[1]);
-    p[2] = s[2] == -INFINITY ? 0.f : fast_exp2(s[2] - U.m[0]);
-    p[3] = s[3] == -INFINITY ? 0.f : fast_exp2(s[3] - U.m[1]);
+}
+
+// Online-softmax step for this thread's 4 candidate scores (rows lo/hi x 2
+// columns, -inf where absent).  The running max moves only when some score of
+// the warp exceeds it by more than 2^8 (lazy rescale), so the common path
+// needs no cross-lane reduction.  Returns the probabilities in p.
+__device__ __forceinline__ void softmax_step(Unit& U, const float s[4], float p[4]) {
+    const bool need = (s[0] > U.m[0] + kLazy) || (s[2] > U.m[0] + kLazy) || (s[1] > U.m[1] + kLazy) ||
+                      (s[3] > U.m[1] + kLazy);
+    if (__any_sync(kFull, need)) raise_max(U, s);
+    // s = -inf gives 0 (a column with no entry yet keeps m = -inf: use 0)
+    const float m0 = U.m[0] == -INFINITY ? 0.f : U.m[0];
+    const float m1 = U.m[1] == -INFINITY ? 0.f : U.m[1];
+    p[0] = fast_exp2(s[0] - m0);
+    p[1] = fast_exp2(s[1] - m1);
+    p[2] = fast_exp2(s[2] - m0);
+    p[3] = fast_exp2(s[3] - m1);
     U.l[0] += p[0] + p[2];
     U.l[1] += p[1] + p[3];
 }
 
-// Window M tile wt of a query pair at tile offset u (query positions i, i + 1):
-// slot rows u + R, R = 16 wt .. 16 wt + 15, hold positions i - W + R.
-__device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, int u, int i, int wt,
-                                            int lane, Unit& U) {
-    const int g8 = lane >> 2, tig = lane & 3, q = tig >> 1;
-    const int W = P.a.W;
+// First probabilities of a row: set the running max to the column max of s
+// (reduced over the 8 threads holding the column); O^T and l are still zero.
+__device__ __forceinline__ void softmax_first(Unit& U, const float s[4], float p[4]) {
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int w = 4; w <= 16; w <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, w));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, w));
+    }
+    U.m[0] = mx0;
+    U.m[1] = mx1;
+    // a column without entries yet keeps m = -inf; its p are 0
+    const float m0 = mx0 == -INFINITY ? 0.f : mx0, m1 = mx1 == -INFINITY ? 0.f : mx1;
+    p[0] = fast_exp2(s[0] - m0);
+    p[1] = fast_exp2(s[1] - m1);
+    p[2] = fast_exp2(s[2] - m0);
+    p[3] = fast_exp2(s[3] - m1);
+    U.l[0] = p[0] + p[2];
+    U.l[1] = p[1] + p[3];
+}
+
+// Window M tile wt of the warp's query quad at tile offset u0 (positions
+// i0 + u0 .. + 3): region rows u0 + R, R = 16 wt .. 16 wt + 15, hold
+// positions i0 + u0 - W + R; unit k holds queries 2k, 2k + 1 of the quad.
+__device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, int u0, int i0, int wt,
+                                            const Lane& L, Unit* U) {
     const int maxr = P.win_rows - 1;
-    const int rk = min(u + 16 * wt + (lane & 7) + (((lane >> 3) & 1) << 3), maxr);
-    const int rv = min(u + 16 * wt + (lane & 7) + ((lane >> 4) << 3), maxr);
-    float c[4];
-    scores(slot + (uint32_t)(rk * PITCH), U, c);
-    float s[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const int R = 16 * wt + g8 + ((e >> 1) << 3);  // M row of this value
-        const bool ok = (R >= q) && (R <= W + q) && (i - W + R >= 0);
-        s[e] = ok ? c[e] : -INFINITY;
+    const int rk = min(u0 + 16 * wt + L.rk, maxr);
+    const int rv = min(u0 + 16 * wt + L.rv, maxr);
+    float c[2][4];
+    scores<2>(slot + (uint32_t)(rk * ROWB), rk, U, c);
+    // window distances of each (row, query); near the sequence start, rows
+    // below lo hold positions before it
+    unsigned mask = L.wmask >> (8 * wt);
+    const int lo = P.a.W - (i0 + u0) - 16 * wt;
+    if (lo > 0) {
+        if (L.g8 < lo) mask &= ~0x33u;          // rows g8 (e = 0, 1) of both units
+        if (L.g8 + 8 < lo) mask &= ~0xccu;      // rows g8 + 8 (e = 2, 3)
     }
-    float p[4];
-    softmax_step(U, s, p);
-    const uint32_t b0 = movm_t(pack_bf16(p[0], p[1]));
-    const uint32_t b1 = movm_t(pack_bf16(p[2], p[3]));
-    accumulate(slot + (uint32_t)((P.win_rows + rv) * PITCH), b0, b1, U);
+    uint32_t b[2][2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float s[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[e] = (mask >> (4 * k + e)) & 1u ? c[k][e] : -INFINITY;
+        float p[4];
+        if (wt == 0)
+            softmax_first(U[k], s, p);
+        else
+            softmax_step(U[k], s, p);
+        b[k][0] = movm_t(pack_bf16(p[0], p[1]));
+        b[k][1] = movm_t(pack_bf16(p[2], p[3]));
+    }
+    accumulate<2>(slot + P.win_region + (uint32_t)(rv * ROWB), rv, b, U);
 }
 
-// Shared-memory address of M row R of a rung tile holding np rungs
-// (R = 3 p + e): rung p's slot row u + e.  The pad row 15 and the rows of
-// absent rungs read a row of rung 0 whose bank group is the one left free.
-__device__ __forceinline__ uint32_t rung_row(int R, int np, int u, uint32_t ring, int rc) {
-    const int p = R / 3;
-    if (R < 15 && p < np) {
-        const int r = u + (R - 3 * p);
-        return ring + ((rc + p) % NRS) * kRungSlotBytes + phase_off(p) + (uint32_t)(r * PITCH);
-    }
-    const int r = (u + 7 <= TQ) ? u + 7 : u - 1;
-    return ring + (rc % NRS) * kRungSlotBytes + (uint32_t)(r * PITCH);
-}
-
-__device__ __forceinline__ void rung_tile(const FwdParams& P, uint32_t ring, int rc, int np, int k0,
-                                          int u, int i, int lane, Unit& U) {
-    const int g8 = lane >> 2, tig = lane & 3, q = tig >> 1;
-    const uint32_t kaddr = rung_row((lane & 7) + (((lane >> 3) & 1) << 3), np, u, ring, rc);
-    const uint32_t vaddr =
-        rung_row((lane & 7) + ((lane >> 4) << 3), np, u, ring, rc) + (uint32_t)(RUNG_ROWS * PITCH);
-    float c[4];
-    scores(kaddr, U, c);
-    // value of the next M row (row a of an interpolation whose row b is this one)
-    const float nx0 = shfl(g8 == 0 ? c[2] : c[0], (lane + 4) & 31);
-    const float nx1 = shfl(g8 == 0 ? c[3] : c[1], (lane + 4) & 31);
-    const float nx2 = shfl(c[2], (lane + 4) & 31);
-    const float nx3 = shfl(c[3], (lane + 4) & 31);
-    const float nx[4] = {nx0, nx1, nx2, nx3};
-    float s[4], tw[2];
+// Rung M tiles of the warp's two query pairs (tile offsets u0 and u0 + 2,
+// positions i0 + u0 ..): np rungs (tile positions 0..np-1 = rungs k0..), rung
+// p in ring slot (rc + p) mod NRS, its block row u + e (e = 0, 1, 2: rows
+// i - n - 1 + e) stored rung_phase(p) rows into the slot.  The pad row 15
+// and rows of absent rungs read a row of rung 0's slot in the swizzle phase
+// no other row of the tile uses.  The two pairs are independent and are
+// interleaved statement by statement.
+__device__ __forceinline__ void rung_tiles(const Smem& S, int rc, int np, int k0, int u0, int i0,
+                                           const Lane& L, Unit* U) {
+    const int lane = threadIdx.x & 31;
+    const int g8 = L.g8;
+    const int hi_k = lane >> 4;
+    const int hi_v = (lane >> 3) & 1;
+    uint32_t krow[2], vrow[2];
+    int kx[2], vx[2];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {  // h = 0: M row g8, h = 1: M row g8 + 8
-        const int R = g8 + 8 * h;
-        const int p = R / 3, e = R - 3 * p;
-        bool useful = (R < 15) && (p < np) && (e == q);
-        float t = 0.f;
-        if (useful) {
-            const Rung rg = P.a.r[k0 + p];
-            t = rg.t;
-            useful = (i + q >= rg.c);
+    for (int k = 0; k < 2; ++k) {
+        const int u = u0 + 2 * k;
+        // pad row: a row TMA wrote for rung 0 (box rows 0..RUNG_ROWS-1) in the
+        // swizzle phase u + 7 that no other row of the tile uses
+        const int pad = (u + 7 <= RUNG_ROWS - 1) ? u + 7 : u - 1;
+        const int ks = L.pk < np ? (rc + L.pk) % NRS : rc % NRS;
+        const int kr = L.pk < np ? u + L.ok : pad;
+        const int vs = L.pv < np ? (rc + L.pv) % NRS : rc % NRS;
+        const int vr = L.pv < np ? u + L.ov : pad;
+        krow[k] = S.rung + ks * kRungSlotBytes + (uint32_t)(kr * ROWB);
+        vrow[k] = S.rung + vs * kRungSlotBytes + kRungRegion + (uint32_t)(vr * ROWB);
+        kx[k] = kr & 7;
+        vx[k] = vr & 7;
+    }
+    // S^T = Khat_rows . Qhat^T, two accumulation chains per pair
+    float c[2][4], d[2][4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[k][e] = d[k][e] = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(krow[k] + (uint32_t)((((2 * s2 + hi_k) ^ kx[k]) & 7) << 4), a0, a1, a2, a3);
+            mma16816((s2 & 1) ? d[k] : c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
         }
-        tw[h] = t;
-        s[2 * h + 0] = useful ? (1.f - t) * nx[2 * h + 0] + t * c[2 * h + 0] : -INFINITY;
-        s[2 * h + 1] = useful ? (1.f - t) * nx[2 * h + 1] + t * c[2 * h + 1] : -INFINITY;
     }
-    float p[4];
-    softmax_step(U, s, p);
-    // p t stays on row b (this row); p (1 - t) moves to row a (the next row)
-    float pa[4], pt[4];
+    // per-row rung data (same for both pairs)
+    const bool use_lo = L.b_lo && L.p_lo < np, use_hi = L.b_hi && L.p_hi < np;
+    SRung rlo{0, 0.f, 0}, rhi{0, 0.f, 0};
+    if (use_lo) rlo = S.r[k0 + L.p_lo];
+    if (use_hi) rhi = S.r[k0 + L.p_hi];
+    uint32_t b[2][2];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        const float t = tw[e >> 1];
-        pa[e] = p[e] * (1.f - t);
-        pt[e] = p[e] * t;
+    for (int k = 0; k < 2; ++k) {
+        const int i = i0 + u0 + 2 * k;
+        float cc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cc[e] = c[k][e] + d[k][e];
+        // value of the next M row (row a of an interpolation whose row b is this one)
+        const float nx0 = shfl(g8 == 0 ? cc[2] : cc[0], (lane + 4) & 31);
+        const float nx1 = shfl(g8 == 0 ? cc[3] : cc[1], (lane + 4) & 31);
+        const float nx2 = shfl(cc[2], (lane + 4) & 31);
+        const float nx3 = shfl(cc[3], (lane + 4) & 31);
+        const bool ul = use_lo && (i + L.q >= rlo.c);
+        const bool uh = use_hi && (i + L.q >= rhi.c);
+        const float tl = rlo.t, th = rhi.t;
+        float sv[4];
+        sv[0] = ul ? (1.f - tl) * nx0 + tl * cc[0] : -INFINITY;
+        sv[1] = ul ? (1.f - tl) * nx1 + tl * cc[1] : -INFINITY;
+        sv[2] = uh ? (1.f - th) * nx2 + th * cc[2] : -INFINITY;
+        sv[3] = uh ? (1.f - th) * nx3 + th * cc[3] : -INFINITY;
+        float p[4];
+        softmax_step(U[k], sv, p);
+        // p t stays on row b (this row); p (1 - t) moves to row a (the next row)
+        const float pa0 = p[0] * (1.f - tl), pa1 = p[1] * (1.f - tl);
+        const float pa2 = p[2] * (1.f - th), pa3 = p[3] * (1.f - th);
+        const float r0 = shfl(pa0, (lane + 28) & 31);
+        const float r1 = shfl(pa1, (lane + 28) & 31);
+        const float r2 = shfl(g8 == 7 ? pa0 : pa2, (lane + 28) & 31);
+        const float r3 = shfl(g8 == 7 ? pa1 : pa3, (lane + 28) & 31);
+        const float lo0 = p[0] * tl + (g8 == 0 ? 0.f : r0);
+        const float lo1 = p[1] * tl + (g8 == 0 ? 0.f : r1);
+        const float hi0 = p[2] * th + r2;
+        const float hi1 = p[3] * th + r3;
+        b[k][0] = movm_t(pack_bf16(lo0, lo1));
+        b[k][1] = movm_t(pack_bf16(hi0, hi1));
     }
-    const float r0 = shfl(pa[0], (lane + 28) & 31);
-    const float r1 = shfl(pa[1], (lane + 28) & 31);
-    const float r2 = shfl(g8 == 7 ? pa[0] : pa[2], (lane + 28) & 31);
-    const float r3 = shfl(g8 == 7 ? pa[1] : pa[3], (lane + 28) & 31);
-    const float lo0 = pt[0] + (g8 == 0 ? 0.f : r0);
-    const float lo1 = pt[1] + (g8 == 0 ? 0.f : r1);
-    const float hi0 = pt[2] + r2;
-    const float hi1 = pt[3] + r3;
-    const uint32_t b0 = movm_t(pack_bf16(lo0, lo1));
-    const uint32_t b1 = movm_t(pack_bf16(hi0, hi1));
-    accumulate(vaddr, b0, b1, U);
+    // O^T += V_rows^T . P^T
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vrow[k] + (uint32_t)((((2 * j + hi_v) ^ vx[k]) & 7) << 4), a0, a1, a2, a3);
+            mma16816(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
+        }
+    }
 }
 
 __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, int u, int lane,
@@ -458,6 +572,7 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
 __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) {
     int wcount = 0, rcount = 0;
     const int u0 = 4 * warp;  // query pairs at tile offsets u0 and u0 + 2
+    const Lane L = make_lane(lane, P.a.W);
     uint32_t raw[2][4][2];
     if (blockIdx.x < P.ntiles) {
         const Tile x = decode(P, blockIdx.x);
@@ -467,6 +582,7 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
     for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
         const Tile x = decode(P, t);
         Unit U[2];
+        int kt;
         {
             const int slot = wcount % NWS;
             bool ok = mbar_wait(bar_full_w(S, slot), (wcount / NWS) & 1, S.abort_flag);
@@ -474,24 +590,20 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
             const uint32_t base = S.win + slot * P.win_slot_bytes;
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                start_unit(P, base + (uint32_t)(2 * P.win_rows * PITCH), x.i0, u0 + 2 * k, lane, raw[k],
-                           U[k]);
+                start_unit(P, base + 2 * P.win_region, x.i0, u0 + 2 * k, lane, raw[k], U[k]);
             // the next tile's Q is in flight while this tile is computed
             if (t + (int)gridDim.x < P.ntiles) {
                 const Tile nx = decode(P, t + gridDim.x);
 #pragma unroll
                 for (int k = 0; k < 2; ++k) fetch_q(P, nx, u0 + 2 * k, lane, raw[k]);
             }
-            for (int wt = 0; wt < P.nwt; ++wt)
-#pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    window_tile(P, base, u0 + 2 * k, x.i0 + u0 + 2 * k, wt, lane, U[k]);
+            for (int wt = 0; wt < P.nwt; ++wt) window_tile(P, base, u0, x.i0, wt, L, U);
+            kt = S.kt[slot];
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty_w(S, slot));
             ++wcount;
         }
         {
-            const int kt = active_rungs(P.a, x.i0);
             for (int k0 = 0; k0 < kt; k0 += RUNGS_PER_TILE) {
                 const int np = min(RUNGS_PER_TILE, kt - k0);
                 bool ok = true;
@@ -500,9 +612,7 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
                     ok = ok && mbar_wait(bar_full_r(S, n % NRS), (n / NRS) & 1, S.abort_flag);
                 }
                 if (!__all_sync(kFull, ok)) goto fail;
-#pragma unroll
-                for (int k = 0; k < 2; ++k)
-                    rung_tile(P, S.rung, rcount, np, k0, u0 + 2 * k, x.i0 + u0 + 2 * k, lane, U[k]);
+                rung_tiles(S, rcount, np, k0, u0, x.i0, L, U);
                 __syncwarp();
                 if (lane == 0)
                     for (int p = 0; p < np; ++p) mbar_arrive(bar_empty_r(S, (rcount + p) % NRS));
@@ -521,13 +631,24 @@ fail:
 }
 
 __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParams P) {
-    extern __shared__ __align__(128) unsigned char smem[];
+    extern __shared__ unsigned char smem_raw[];
+    // the dynamic allocation carries 1024 spare bytes to reach 1024 alignment
+    const uint32_t raw_base = smem_u32(smem_raw);
+    const uint32_t base = (raw_base + 1023u) & ~1023u;
+    unsigned char* hdr = smem_raw + (base - raw_base);
     Smem S;
-    S.bars = smem_u32(smem);
-    S.abort_flag = reinterpret_cast<int*>(smem + kBarBytes);
-    S.win = smem_u32(smem) + kHeaderBytes;
+    S.bars = base;
+    S.abort_flag = reinterpret_cast<int*>(hdr + kFlagOffset);
+    S.kt = reinterpret_cast<int*>(hdr + kKtOffset);
+    SRung* table = reinterpret_cast<SRung*>(hdr + kRungTableOffset);
+    S.r = table;
+    S.win = base + kHeaderBytes;
     S.rung = S.win + NWS * P.win_slot_bytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x < P.a.nr) {
+        const Rung rg = P.a.r[threadIdx.x];
+        table[threadIdx.x] = SRung{rg.n, rg.t, rg.c};
+    }
     if (threadIdx.x == 0) {
         // full: one arrival (the producer's expect_tx) plus the copied bytes;
         // empty: one arrival per consumer warp
@@ -543,10 +664,11 @@ __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParam
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    if (warp == NCW)
-        producer(P, S, lane);
-    else
+    if (warp == NCW) {
+        if (lane == 0) producer(P, S);
+    } else {
         consumer(P, S, warp, lane);
+    }
 }
 
 // -------------------------------------------------- RoPE on the keys
@@ -579,6 +701,8 @@ __global__ void __launch_bounds__(256) rope_k_kernel(const __nv_bfloat16* __rest
     *reinterpret_cast<uint4*>(khat + row * kD + kPairs + 8 * c) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
 }
 
+// ------------------------------------------------------------- host side
+
 struct DeviceInfo {
     int sms = 0;
     size_t configured_smem = 0;
@@ -587,6 +711,34 @@ struct DeviceInfo {
 DeviceInfo& device_info(int dev) {
     static DeviceInfo info[64];
     return info[dev & 63];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    return fn;
+}
+
+// 4-D map over a [B][T][Hkv][64] bf16 tensor (innermost first: d, g, t, b),
+// box of `rows` rows of one head, 128-byte swizzle, zero fill outside.
+bool encode_rows(CUtensorMap* m, const void* base, int B, int T, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHkv, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kHkv * kD * 2,
+                                   (cuuint64_t)T * kHkv * kD * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)kD, 1u, (cuuint32_t)rows, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -609,9 +761,9 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
         if (e != cudaSuccess) return e;
     }
     FwdParams P;
+    std::memset(&P, 0, sizeof(P));
     P.a = a;
     P.q = static_cast<const __nv_bfloat16*>(q);
-    P.v = static_cast<const __nv_bfloat16*>(v);
     P.o = static_cast<__nv_bfloat16*>(o);
     P.lse = lse;
     P.status = status;
@@ -619,8 +771,10 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.ntq = (a.T + TQ - 1) / TQ;
     P.ntiles = a.B * P.ntq * kHkv;
     P.win_rows = TQ + a.W;
-    P.nwt = (a.W + 2 + 15) / 16;
-    P.win_slot_bytes = (unsigned)(((2 * P.win_rows * PITCH + TQ * TABB) + 127) & ~127);
+    P.nwt = (a.W + 4 + 15) / 16;
+    P.win_region = round1k((unsigned)P.win_rows * ROWB);
+    P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
+    const void* khat = k;
     if (rope) {
         const long long rows = (long long)a.B * a.T * kHkv;
         const long long threads = rows * 4;
@@ -628,11 +782,17 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
             static_cast<const __nv_bfloat16*>(k), rope, static_cast<__nv_bfloat16*>(ws), rows, a.T);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         count_launch();
-        P.khat = static_cast<const __nv_bfloat16*>(ws);
-    } else {
-        P.khat = static_cast<const __nv_bfloat16*>(k);
+        khat = ws;
     }
-    const size_t smem = kHeaderBytes + NWS * (size_t)P.win_slot_bytes + NRS * (size_t)kRungSlotBytes;
+    if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) ||
+        !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows))
+        return cudaErrorInvalidValue;
+    for (int p = 0; p < RUNGS_PER_TILE; ++p) {
+        const int rows = RUNG_ROWS + ((3 * p) & 7);
+        if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, rows) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, rows))
+            return cudaErrorInvalidValue;
+    }
+    const size_t smem = 1024 + kHeaderBytes + NWS * (size_t)P.win_slot_bytes + NRS * (size_t)kRungSlotBytes;
     if (info.configured_smem < smem) {
         e = cudaFuncSetAttribute(fwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -1,5 +1,5 @@
 // sfa_mma.cuh -- inline-PTX helpers shared by the tensor-core kernels of
-// libsfa (mbarrier ring, TMA bulk copies, ldmatrix, mma.sync, movmatrix).
+// libsfa (mbarrier ring, TMA copies, ldmatrix, mma.sync, movmatrix).
 // Private to the CUDA library.
 #pragma once
 
@@ -65,6 +65,18 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
             dst),
         "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// One tiled TMA load of a 4-D box (coordinates innermost first) into shared
+// memory, completion counted on the mbarrier.  The innermost coordinate must
+// be a multiple of 16 bytes; out-of-range boxes are zero filled.
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
 
