@@ -53,8 +53,8 @@ using namespace mma;
 constexpr int TQ = 28;                 // queries per tile
 constexpr int NCW = 7;                 // consumer warps (2 query pairs each)
 constexpr int NTHREADS = (NCW + 1) * 32;
-constexpr int NRS = 7;                 // rung slots
-constexpr int NWS = 2;                 // window slots
+constexpr int NRS = 8;                 // rung slots
+constexpr int NWS = 1;                 // window slots (free again after the window phase)
 constexpr int MAXPH = 7;               // largest box offset of a rung position
 constexpr int RUNG_ROWS = TQ + 1;      // rows a rung block needs
 constexpr int RUNG_BOX = RUNG_ROWS + MAXPH;
@@ -69,12 +69,14 @@ constexpr unsigned round1k(unsigned x) { return (x + 1023u) & ~1023u; }
 constexpr unsigned kRungRegion = round1k(RUNG_BOX * ROWB);  // one tensor of a rung slot
 constexpr unsigned kRungSlotBytes = 2 * kRungRegion;        // Khat region, then V region
 constexpr unsigned kHeaderBytes = 1024;                     // barriers, flag, rung table
+constexpr unsigned kObufBytes = 2 * 8 * ROWB;                // per consumer warp: O of 2 query pairs
 
 struct FwdParams {
     CUtensorMap kmap_w;      // Khat, box of win_rows rows
     CUtensorMap vmap_w;      // V, box of win_rows rows
     CUtensorMap kmap_r[5];   // Khat, box of RUNG_ROWS + rung_phase(p) rows, rung position p
     CUtensorMap vmap_r[5];   // V, same boxes
+    CUtensorMap omap;        // O [B][T][8][64], box of 2 queries x 4 heads, 128-byte swizzle
     LayerArgs a;
     const __nv_bfloat16* q;
     const float2* rope;      // nullptr: Q is used as given
@@ -114,13 +116,20 @@ struct SRung {
     int c;
 };
 
+struct TC {
+    float t;
+    int c;
+};
+
 struct Smem {
     uint32_t bars;      // full_w[NWS], empty_w[NWS], full_r[NRS], empty_r[NRS]
     uint32_t win;       // NWS window slots
     uint32_t rung;      // NRS rung slots
+    uint32_t obuf;      // NCW output staging buffers
     int* abort_flag;
     int* kt;            // per window slot: rungs usable by the slot's tile
     const SRung* r;     // the kept rungs, by increasing distance
+    uint32_t tc;        // shared address of TC[nr] (t and ceil of each kept rung)
 };
 
 __device__ __forceinline__ uint32_t bar_full_w(const Smem& s, int i) { return s.bars + 8 * i; }
@@ -133,8 +142,9 @@ constexpr int kBarBytes = 8 * 2 * (NWS + NRS);
 constexpr int kFlagOffset = kBarBytes;
 constexpr int kKtOffset = kFlagOffset + 4;   // per window slot: rungs usable by its tile
 constexpr int kRungTableOffset = 256;
+constexpr int kTcOffset = kRungTableOffset + SFA_MAX_RUNGS * 12;  // {t, ceil} per rung, 8 bytes
 static_assert(kKtOffset + 4 * NWS <= kRungTableOffset, "header overflow");
-static_assert(kRungTableOffset + SFA_MAX_RUNGS * 12 <= (int)kHeaderBytes, "header overflow");
+static_assert(kTcOffset + SFA_MAX_RUNGS * 8 <= (int)kHeaderBytes, "header overflow");
 
 // Rungs are sorted by ceil(d): those usable by some query of the tile form a prefix.
 __device__ __forceinline__ int active_rungs(const Smem& S, int nr, int i0) {
@@ -168,7 +178,7 @@ __device__ void producer(const FwdParams& P, const Smem& S) {
         {
             const int kt = S.kt[(wcount - 1) % NWS];
             for (int k = 0; k < kt; ++k) {
-                const int slot = rcount % NRS;
+                const int slot = rcount & (NRS - 1);
                 if (!mbar_wait(bar_empty_r(S, slot), ((rcount / NRS) & 1) ^ 1, S.abort_flag)) goto fail;
                 const uint32_t base = S.rung + slot * kRungSlotBytes;
                 const uint32_t full = bar_full_r(S, slot);
@@ -196,6 +206,30 @@ fail:
 
 // ------------------------------------------------------------ consumers
 
+// Warp-uniform bounded wait (every lane polls, the warp leaves together).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+    const unsigned long long t0 = now_ns();
+    for (unsigned it = 0;; ++it) {
+        if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
+        if (__any_sync(kFull, *abort_flag != 0)) return false;
+        if ((it & 15) == 15 && __any_sync(kFull, now_ns() - t0 > kWaitNs)) return false;
+        __nanosleep(32);
+    }
+}
+
+__device__ __forceinline__ TC lds_tc(uint32_t addr) {
+    TC v;
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=f"(v.t), "=r"(v.c) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
 // One query pair (i, i + 1) of one key/value head: the B fragments of
 // Qhat^T (scaled into log2 units), the O^T accumulators and softmax state of
 // this thread's two columns (query tig/2, heads 2(tig&1) and 2(tig&1)+1).
@@ -203,90 +237,54 @@ struct Unit {
     uint32_t qf[4][2];
     float o[4][4];
     float m[2];
+    float th[2];   // m + lazy margin: a score above it raises the running max
     float l[2];
 };
 
-// Raw Q of this thread's B-fragment column (query i0 + u + g8/4, head
-// g*4 + g8%4): dimensions 16 s + 8 h + 2 tig + {0, 1}.
-__device__ __forceinline__ void fetch_q(const FwdParams& P, const Tile& x, int u, int lane,
-                                        uint32_t raw[4][2]) {
-    const int g8 = lane >> 2, tig = lane & 3;
-    const int iq = x.i0 + u + (g8 >> 2);
-    if (iq < P.a.T) {
-        const __nv_bfloat16* qp =
-            P.q + (((size_t)x.b * P.a.T + iq) * kHq + x.g * kG + (g8 & 3)) * kD + 2 * tig;
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-            raw[s][0] = __ldg(reinterpret_cast<const unsigned*>(qp + 16 * s));
-            raw[s][1] = __ldg(reinterpret_cast<const unsigned*>(qp + 16 * s + 8));
-        }
-    } else {
-#pragma unroll
-        for (int s = 0; s < 4; ++s) raw[s][0] = raw[s][1] = 0u;
-    }
-}
-
-// Rotate (RoPE rows of the tile in shared memory at `tab`) and scale the raw
-// Q into B fragments; reset the accumulators.
-__device__ __forceinline__ void start_unit(const FwdParams& P, uint32_t tab, int i0, int u, int lane,
-                                           const uint32_t raw[4][2], Unit& U) {
-    const int g8 = lane >> 2, tig = lane & 3;
-    const float sl2 = P.a.scale * kLog2e;
-    // RoPE rows are staged only for positions < T
-    const bool rot = P.rope && (i0 + u + (g8 >> 2) < P.a.T);
-    const uint32_t trow = tab + (uint32_t)((u + (g8 >> 2)) * TABB + 2 * tig * 8);
-#pragma unroll
-    for (int s = 0; s < 2; ++s) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            // dims m = 16 s + 8 h + 2 tig + {0, 1} and their partners m + 32
-            float4 cs = make_float4(1.f, 0.f, 1.f, 0.f);
-            if (rot) {
-                asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                             : "=f"(cs.x), "=f"(cs.y), "=f"(cs.z), "=f"(cs.w)
-                             : "r"(trow + (uint32_t)((16 * s + 8 * h) * 8)));
-            }
-            const float2 xv = unpack_bf16(raw[s][h]);
-            const float2 yv = unpack_bf16(raw[s + 2][h]);
-            const float x0 = (xv.x * cs.x - yv.x * cs.y) * sl2;
-            const float y0 = (yv.x * cs.x + xv.x * cs.y) * sl2;
-            const float x1 = (xv.y * cs.z - yv.y * cs.w) * sl2;
-            const float y1 = (yv.y * cs.z + xv.y * cs.w) * sl2;
-            U.qf[s][h] = pack_bf16(x0, x1);
-            U.qf[s + 2][h] = pack_bf16(y0, y1);
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) U.o[j][e] = 0.f;
-    U.m[0] = U.m[1] = -INFINITY;
-    U.l[0] = U.l[1] = 0.f;
-}
-
-// Per-thread constants of the M-tile layouts (independent of the tile).
+// Per-thread constants of the fragment layouts (fixed for the whole kernel:
+// the warp always owns the query pairs at tile offsets u0 and u0 + 2).
+// Addresses are byte offsets inside a slot region, with the 128-byte swizzle
+// of ldmatrix k-step (or m tile) 0 folded in: step s reads at offset ^ (s << 5).
 struct Lane {
-    int g8, tig, q;   // fragment row group, column pair, query of this thread's C columns
-    int rk, rv;       // M row this lane feeds to ldmatrix: Khat (A) and V (A, .trans)
-    int pk, pv;       // rung position of those rows in a rung tile (5: the pad row)
-    int ok, ov;       // their region-row offset from u (e + phase; unused for the pad row)
-    int p_lo, p_hi;   // rung position of this thread's C rows g8 and g8 + 8
-    bool b_lo, b_hi;  // the row is row b of query q's interpolation (e == q, not the pad)
-    unsigned wmask;   // window: bit (8 wt + 4 k + e) set when M row 16 wt + g8 + 8 (e/2)
-                      // is a window distance of quad query 2k + q (before the start check)
+    int g8, q;          // fragment row group; query of this thread's C columns
+    int pk, pv;         // rung position of the rows this lane feeds to ldmatrix (5: pad)
+    int p_lo, p_hi;     // rung position of this thread's C rows g8 and g8 + 8
+    bool b_lo, b_hi;    // that row is row b of query q's interpolation
+    unsigned wmask;     // window: bit (8 wt + 4 k + e) = row is a window distance of
+                        // quad query 2k + q (before the sequence-start check)
+    uint32_t kr[2], krp[2];   // rung tiles, unit k: Khat row offset (rung row / pad row)
+    uint32_t vr[2], vrp[2];   // rung tiles, unit k: V row offset (rung row / pad row)
+    uint32_t wk, wv;          // window tile 0: Khat and V row offsets
+    uint32_t ob[2];           // output staging: stmatrix row address offsets (jj = 0, 1)
 };
 
-__device__ __forceinline__ Lane make_lane(int lane, int W) {
+__device__ __forceinline__ uint32_t swz_row(int r, int hi) {
+    return (uint32_t)(r * ROWB) + (uint32_t)(((hi ^ r) & 7) << 4);
+}
+
+__device__ __forceinline__ Lane make_lane(int lane, int u0, int W, int win_rows) {
     Lane L;
     L.g8 = lane >> 2;
-    L.tig = lane & 3;
-    L.q = L.tig >> 1;
-    L.rk = (lane & 7) + (((lane >> 3) & 1) << 3);
-    L.rv = (lane & 7) + ((lane >> 4) << 3);
-    L.pk = L.rk < 15 ? L.rk / 3 : 5;
-    L.pv = L.rv < 15 ? L.rv / 3 : 5;
-    L.ok = L.rk < 15 ? L.rk - 3 * L.pk + rung_phase(L.pk) : 7;
-    L.ov = L.rv < 15 ? L.rv - 3 * L.pv + rung_phase(L.pv) : 7;
+    L.q = (lane & 3) >> 1;
+    const int hk = lane >> 4, hv = (lane >> 3) & 1;
+    const int rk = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int rv = (lane & 7) + ((lane >> 4) << 3);
+    L.pk = rk < 15 ? rk / 3 : 5;
+    L.pv = rv < 15 ? rv / 3 : 5;
+    const int ok = rk < 15 ? rk - 3 * L.pk + rung_phase(L.pk) : 0;
+    const int ov = rv < 15 ? rv - 3 * L.pv + rung_phase(L.pv) : 0;
+    for (int k = 0; k < 2; ++k) {
+        const int u = u0 + 2 * k;
+        // pad row: a row TMA wrote for rung 0 (box rows 0..RUNG_ROWS-1) in the
+        // swizzle phase u + 7 that no other row of the tile uses
+        const int pad = (u + 7 <= RUNG_ROWS - 1) ? u + 7 : u - 1;
+        L.kr[k] = swz_row(u + ok, hk);
+        L.krp[k] = swz_row(pad, hk);
+        L.vr[k] = swz_row(u + ov, hv);
+        L.vrp[k] = swz_row(pad, hv);
+    }
+    L.wk = swz_row(min(u0 + rk, win_rows - 1), hk);
+    L.wv = swz_row(min(u0 + rv, win_rows - 1), hv);
     const int rlo = L.g8, rhi = L.g8 + 8;
     L.p_lo = rlo / 3;
     L.p_hi = rhi < 15 ? rhi / 3 : 5;
@@ -300,44 +298,90 @@ __device__ __forceinline__ Lane make_lane(int lane, int W) {
                 const int qq = 2 * k + L.q;
                 if (R >= qq && R <= W + qq) L.wmask |= 1u << (8 * wt + 4 * k + e);
             }
+    // stmatrix: stored matrix mi = lane >> 3 of call jj is (m tile 2 jj + mi/2,
+    // half mi & 1); this lane gives its row (lane & 7) = output row (query, head)
+    const int row = lane & 7, mi = lane >> 3;
+    for (int jj = 0; jj < 2; ++jj) {
+        const int chunk = 2 * (2 * jj + (mi >> 1)) + (mi & 1);
+        L.ob[jj] = (uint32_t)(row * ROWB) + (uint32_t)(((chunk ^ row) & 7) << 4);
+    }
     return L;
 }
 
-// S^T (16 rows x 8 columns) = Khat rows . Qhat^T for the units in U[0..NU).
-// This lane feeds ldmatrix row L.rk of the tile: region row r at `row`.
-template <int NU>
-__device__ __forceinline__ void scores(uint32_t row, int r, const Unit* U, float c[][4]) {
+// Raw Q of this thread's B-fragment column (query i0 + u + g8/4, head
+// g*4 + g8%4): dimensions 16 s + 8 h + 2 tig + {0, 1}.
+__device__ __forceinline__ void fetch_q(const FwdParams& P, const Tile& x, int u, int lane,
+                                        uint32_t raw[4][2]) {
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int iq = min(x.i0 + u + (g8 >> 2), P.a.T - 1);  // rows past the end are not stored
+    const __nv_bfloat16* qp =
+        P.q + (((size_t)x.b * P.a.T + iq) * kHq + x.g * kG + (g8 & 3)) * kD + 2 * tig;
 #pragma unroll
-    for (int k = 0; k < NU; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = 0.f;
-    const int hi = (threadIdx.x & 31) >> 4;
-    const int x = r & 7;
-#pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4(row + (uint32_t)((((2 * s + hi) ^ x) & 7) << 4), a0, a1, a2, a3);
-#pragma unroll
-        for (int k = 0; k < NU; ++k) mma16816(c[k], a0, a1, a2, a3, U[k].qf[s][0], U[k].qf[s][1]);
+    for (int s2 = 0; s2 < 4; ++s2) {
+        raw[s2][0] = __ldg(reinterpret_cast<const unsigned*>(qp + 16 * s2));
+        raw[s2][1] = __ldg(reinterpret_cast<const unsigned*>(qp + 16 * s2 + 8));
     }
 }
 
-// O^T += V_rows^T . P^T for the units in U[0..NU), P^T given as bf16 B
-// fragments b[k][0] (rows 0-7), b[k][1] (rows 8-15).  This lane feeds
-// ldmatrix row L.rv.
-template <int NU>
-__device__ __forceinline__ void accumulate(uint32_t row, int r, const uint32_t b[][2], Unit* U) {
-    const int hi = ((threadIdx.x & 31) >> 3) & 1;
-    const int x = r & 7;
+// Rotate (RoPE rows of the tile in shared memory at `tab`, nq of them) and
+// scale the raw Q into B fragments; reset the accumulators.
+__device__ __forceinline__ void start_unit(const FwdParams& P, uint32_t tab, int nq, int u, int lane,
+                                           const uint32_t raw[4][2], Unit& U) {
+    const int g8 = lane >> 2, tig = lane & 3;
+    const float sl2 = P.a.scale * kLog2e;
+    const uint32_t trow = tab + (uint32_t)(min(u + (g8 >> 2), nq - 1) * TABB + 2 * tig * 8);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        uint32_t a0, a1, a2, a3;
-        ldsm_x4_t(row + (uint32_t)((((2 * j + hi) ^ x) & 7) << 4), a0, a1, a2, a3);
+    for (int s2 = 0; s2 < 2; ++s2) {
 #pragma unroll
-        for (int k = 0; k < NU; ++k) mma16816(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
+        for (int h = 0; h < 2; ++h) {
+            // dims m = 16 s + 8 h + 2 tig + {0, 1} and their partners m + 32
+            float4 cs = make_float4(sl2, 0.f, sl2, 0.f);
+            if (P.rope) {
+                cs = lds_f4(trow + (uint32_t)((16 * s2 + 8 * h) * 8));
+                cs.x *= sl2;
+                cs.y *= sl2;
+                cs.z *= sl2;
+                cs.w *= sl2;
+            }
+            const float2 xv = unpack_bf16(raw[s2][h]);
+            const float2 yv = unpack_bf16(raw[s2 + 2][h]);
+            U.qf[s2][h] = pack_bf16(xv.x * cs.x - yv.x * cs.y, xv.y * cs.z - yv.y * cs.w);
+            U.qf[s2 + 2][h] = pack_bf16(yv.x * cs.x + xv.x * cs.y, yv.y * cs.z + xv.y * cs.w);
+        }
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) U.o[j][e] = 0.f;
+}
+
+// The next tile's raw Q is fetched while this tile is computed.
+
+// Softmax of the first window entries of a row: the running max becomes the
+// column max of s (reduced over the 8 threads holding the column).
+__device__ __forceinline__ void softmax_first(Unit& U, const float s[4], float p[4]) {
+    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
+#pragma unroll
+    for (int w = 4; w <= 16; w <<= 1) {
+        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, w));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, w));
+    }
+    U.m[0] = mx0;
+    U.m[1] = mx1;
+    U.th[0] = mx0 + kLazy;
+    U.th[1] = mx1 + kLazy;
+    // a column without entries yet keeps m = -inf; its p are 0
+    const float m0 = mx0 == -INFINITY ? 0.f : mx0, m1 = mx1 == -INFINITY ? 0.f : mx1;
+    p[0] = fast_exp2(s[0] - m0);
+    p[1] = fast_exp2(s[1] - m1);
+    p[2] = fast_exp2(s[2] - m0);
+    p[3] = fast_exp2(s[3] - m1);
+    U.l[0] = p[0] + p[2];
+    U.l[1] = p[1] + p[3];
 }
 
 // Raise the running max of this thread's two columns to the column max of s
-// (reduced over the 8 threads holding the column) and rescale O^T and l.
+// and rescale O^T and l.
 __device__ __forceinline__ void raise_max(Unit& U, const float s[4]) {
     float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
@@ -350,6 +394,8 @@ __device__ __forceinline__ void raise_max(Unit& U, const float s[4]) {
     const float c1 = (U.m[1] == -INFINITY) ? (n1 == -INFINITY ? 1.f : 0.f) : fast_exp2(U.m[1] - n1);
     U.m[0] = n0;
     U.m[1] = n1;
+    U.th[0] = n0 + kLazy;
+    U.th[1] = n1 + kLazy;
     U.l[0] *= c0;
     U.l[1] *= c1;
 #pragma unroll
@@ -361,15 +407,11 @@ __device__ __forceinline__ void raise_max(Unit& U, const float s[4]) {
     }
 }
 
-// Online-softmax step for this thread's 4 candidate scores (rows lo/hi x 2
-// columns, -inf where absent).  The running max moves only when some score of
-// the warp exceeds it by more than 2^8 (lazy rescale), so the common path
-// needs no cross-lane reduction.  Returns the probabilities in p.
+// Online-softmax step (lazy: the running max moves only when a score of the
+// warp exceeds it by more than 2^8).  Returns the probabilities in p.
 __device__ __forceinline__ void softmax_step(Unit& U, const float s[4], float p[4]) {
-    const bool need = (s[0] > U.m[0] + kLazy) || (s[2] > U.m[0] + kLazy) || (s[1] > U.m[1] + kLazy) ||
-                      (s[3] > U.m[1] + kLazy);
+    const bool need = (s[0] > U.th[0]) || (s[2] > U.th[0]) || (s[1] > U.th[1]) || (s[3] > U.th[1]);
     if (__any_sync(kFull, need)) raise_max(U, s);
-    // s = -inf gives 0 (a column with no entry yet keeps m = -inf: use 0)
     const float m0 = U.m[0] == -INFINITY ? 0.f : U.m[0];
     const float m1 = U.m[1] == -INFINITY ? 0.f : U.m[1];
     p[0] = fast_exp2(s[0] - m0);
@@ -380,37 +422,28 @@ __device__ __forceinline__ void softmax_step(Unit& U, const float s[4], float p[
     U.l[1] += p[1] + p[3];
 }
 
-// First probabilities of a row: set the running max to the column max of s
-// (reduced over the 8 threads holding the column); O^T and l are still zero.
-__device__ __forceinline__ void softmax_first(Unit& U, const float s[4], float p[4]) {
-    float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
-#pragma unroll
-    for (int w = 4; w <= 16; w <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, w));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, w));
-    }
-    U.m[0] = mx0;
-    U.m[1] = mx1;
-    // a column without entries yet keeps m = -inf; its p are 0
-    const float m0 = mx0 == -INFINITY ? 0.f : mx0, m1 = mx1 == -INFINITY ? 0.f : mx1;
-    p[0] = fast_exp2(s[0] - m0);
-    p[1] = fast_exp2(s[1] - m1);
-    p[2] = fast_exp2(s[2] - m0);
-    p[3] = fast_exp2(s[3] - m1);
-    U.l[0] = p[0] + p[2];
-    U.l[1] = p[1] + p[3];
-}
-
 // Window M tile wt of the warp's query quad at tile offset u0 (positions
 // i0 + u0 .. + 3): region rows u0 + R, R = 16 wt .. 16 wt + 15, hold
 // positions i0 + u0 - W + R; unit k holds queries 2k, 2k + 1 of the quad.
 __device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, int u0, int i0, int wt,
                                             const Lane& L, Unit* U) {
-    const int maxr = P.win_rows - 1;
-    const int rk = min(u0 + 16 * wt + L.rk, maxr);
-    const int rv = min(u0 + 16 * wt + L.rv, maxr);
+    const int lane = threadIdx.x & 31;
+    uint32_t kro = L.wk, vro = L.wv;
+    if (wt > 0) {
+        const int maxr = P.win_rows - 1;
+        kro = swz_row(min(u0 + 16 * wt + (lane & 7) + (((lane >> 3) & 1) << 3), maxr), lane >> 4);
+        vro = swz_row(min(u0 + 16 * wt + (lane & 7) + ((lane >> 4) << 3), maxr), (lane >> 3) & 1);
+    }
     float c[2][4];
-    scores<2>(slot + (uint32_t)(rk * ROWB), rk, U, c);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = 0.f;
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(slot + (kro ^ (uint32_t)(s2 << 5)), a0, a1, a2, a3);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) mma16816(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+    }
     // window distances of each (row, query); near the sequence start, rows
     // below lo hold positions before it
     unsigned mask = L.wmask >> (8 * wt);
@@ -422,18 +455,25 @@ __device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, i
     uint32_t b[2][2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        float s[4];
+        float sv[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) s[e] = (mask >> (4 * k + e)) & 1u ? c[k][e] : -INFINITY;
+        for (int e = 0; e < 4; ++e) sv[e] = (mask >> (4 * k + e)) & 1u ? c[k][e] : -INFINITY;
         float p[4];
         if (wt == 0)
-            softmax_first(U[k], s, p);
+            softmax_first(U[k], sv, p);
         else
-            softmax_step(U[k], s, p);
+            softmax_step(U[k], sv, p);
         b[k][0] = movm_t(pack_bf16(p[0], p[1]));
         b[k][1] = movm_t(pack_bf16(p[2], p[3]));
     }
-    accumulate<2>(slot + P.win_region + (uint32_t)(rv * ROWB), rv, b, U);
+    const uint32_t vbase = slot + P.win_region;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vbase + (vro ^ (uint32_t)(j << 5)), a0, a1, a2, a3);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) mma16816(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
+    }
 }
 
 // Rung M tiles of the warp's two query pairs (tile offsets u0 and u0 + 2,
@@ -441,30 +481,20 @@ __device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, i
 // p in ring slot (rc + p) mod NRS, its block row u + e (e = 0, 1, 2: rows
 // i - n - 1 + e) stored rung_phase(p) rows into the slot.  The pad row 15
 // and rows of absent rungs read a row of rung 0's slot in the swizzle phase
-// no other row of the tile uses.  The two pairs are independent and are
-// interleaved statement by statement.
-__device__ __forceinline__ void rung_tiles(const Smem& S, int rc, int np, int k0, int u0, int i0,
+// no other row of the tile uses.  The two pairs are interleaved.
+__device__ __forceinline__ void rung_tiles(const Smem& S, int rc, int np, int k0, int nr, int u0, int i0,
                                            const Lane& L, Unit* U) {
     const int lane = threadIdx.x & 31;
     const int g8 = L.g8;
-    const int hi_k = lane >> 4;
-    const int hi_v = (lane >> 3) & 1;
+    const bool kin = L.pk < np, vin = L.pv < np;
+    const uint32_t kslot = S.rung + (uint32_t)(((rc + (kin ? L.pk : 0)) & (NRS - 1)) * kRungSlotBytes);
+    const uint32_t vslot =
+        S.rung + kRungRegion + (uint32_t)(((rc + (vin ? L.pv : 0)) & (NRS - 1)) * kRungSlotBytes);
     uint32_t krow[2], vrow[2];
-    int kx[2], vx[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
-        const int u = u0 + 2 * k;
-        // pad row: a row TMA wrote for rung 0 (box rows 0..RUNG_ROWS-1) in the
-        // swizzle phase u + 7 that no other row of the tile uses
-        const int pad = (u + 7 <= RUNG_ROWS - 1) ? u + 7 : u - 1;
-        const int ks = L.pk < np ? (rc + L.pk) % NRS : rc % NRS;
-        const int kr = L.pk < np ? u + L.ok : pad;
-        const int vs = L.pv < np ? (rc + L.pv) % NRS : rc % NRS;
-        const int vr = L.pv < np ? u + L.ov : pad;
-        krow[k] = S.rung + ks * kRungSlotBytes + (uint32_t)(kr * ROWB);
-        vrow[k] = S.rung + vs * kRungSlotBytes + kRungRegion + (uint32_t)(vr * ROWB);
-        kx[k] = kr & 7;
-        vx[k] = vr & 7;
+        krow[k] = kslot + (kin ? L.kr[k] : L.krp[k]);
+        vrow[k] = vslot + (vin ? L.vr[k] : L.vrp[k]);
     }
     // S^T = Khat_rows . Qhat^T, two accumulation chains per pair
     float c[2][4], d[2][4];
@@ -477,15 +507,15 @@ __device__ __forceinline__ void rung_tiles(const Smem& S, int rc, int np, int k0
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4(krow[k] + (uint32_t)((((2 * s2 + hi_k) ^ kx[k]) & 7) << 4), a0, a1, a2, a3);
+            ldsm_x4(krow[k] ^ (uint32_t)(s2 << 5), a0, a1, a2, a3);
             mma16816((s2 & 1) ? d[k] : c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
         }
     }
-    // per-row rung data (same for both pairs)
+    // t and ceil of the rungs of this thread's rows (same for both pairs)
+    const TC rlo = lds_tc(S.tc + (uint32_t)(min(k0 + L.p_lo, nr - 1) * 8));
+    const TC rhi = lds_tc(S.tc + (uint32_t)(min(k0 + L.p_hi, nr - 1) * 8));
     const bool use_lo = L.b_lo && L.p_lo < np, use_hi = L.b_hi && L.p_hi < np;
-    SRung rlo{0, 0.f, 0}, rhi{0, 0.f, 0};
-    if (use_lo) rlo = S.r[k0 + L.p_lo];
-    if (use_hi) rhi = S.r[k0 + L.p_hi];
+    const float tl = rlo.t, th = rhi.t;
     uint32_t b[2][2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
@@ -500,27 +530,22 @@ __device__ __forceinline__ void rung_tiles(const Smem& S, int rc, int np, int k0
         const float nx3 = shfl(cc[3], (lane + 4) & 31);
         const bool ul = use_lo && (i + L.q >= rlo.c);
         const bool uh = use_hi && (i + L.q >= rhi.c);
-        const float tl = rlo.t, th = rhi.t;
         float sv[4];
-        sv[0] = ul ? (1.f - tl) * nx0 + tl * cc[0] : -INFINITY;
-        sv[1] = ul ? (1.f - tl) * nx1 + tl * cc[1] : -INFINITY;
-        sv[2] = uh ? (1.f - th) * nx2 + th * cc[2] : -INFINITY;
-        sv[3] = uh ? (1.f - th) * nx3 + th * cc[3] : -INFINITY;
+        sv[0] = ul ? fmaf(tl, cc[0] - nx0, nx0) : -INFINITY;
+        sv[1] = ul ? fmaf(tl, cc[1] - nx1, nx1) : -INFINITY;
+        sv[2] = uh ? fmaf(th, cc[2] - nx2, nx2) : -INFINITY;
+        sv[3] = uh ? fmaf(th, cc[3] - nx3, nx3) : -INFINITY;
         float p[4];
         softmax_step(U[k], sv, p);
         // p t stays on row b (this row); p (1 - t) moves to row a (the next row)
-        const float pa0 = p[0] * (1.f - tl), pa1 = p[1] * (1.f - tl);
-        const float pa2 = p[2] * (1.f - th), pa3 = p[3] * (1.f - th);
+        const float pt0 = p[0] * tl, pt1 = p[1] * tl, pt2 = p[2] * th, pt3 = p[3] * th;
+        const float pa0 = p[0] - pt0, pa1 = p[1] - pt1, pa2 = p[2] - pt2, pa3 = p[3] - pt3;
         const float r0 = shfl(pa0, (lane + 28) & 31);
         const float r1 = shfl(pa1, (lane + 28) & 31);
         const float r2 = shfl(g8 == 7 ? pa0 : pa2, (lane + 28) & 31);
         const float r3 = shfl(g8 == 7 ? pa1 : pa3, (lane + 28) & 31);
-        const float lo0 = p[0] * tl + (g8 == 0 ? 0.f : r0);
-        const float lo1 = p[1] * tl + (g8 == 0 ? 0.f : r1);
-        const float hi0 = p[2] * th + r2;
-        const float hi1 = p[3] * th + r3;
-        b[k][0] = movm_t(pack_bf16(lo0, lo1));
-        b[k][1] = movm_t(pack_bf16(hi0, hi1));
+        b[k][0] = movm_t(pack_bf16(g8 == 0 ? pt0 : pt0 + r0, g8 == 0 ? pt1 : pt1 + r1));
+        b[k][1] = movm_t(pack_bf16(pt2 + r2, pt3 + r3));
     }
     // O^T += V_rows^T . P^T
 #pragma unroll
@@ -528,14 +553,17 @@ __device__ __forceinline__ void rung_tiles(const Smem& S, int rc, int np, int k0
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(vrow[k] + (uint32_t)((((2 * j + hi_v) ^ vx[k]) & 7) << 4), a0, a1, a2, a3);
+            ldsm_x4_t(vrow[k] ^ (uint32_t)(j << 5), a0, a1, a2, a3);
             mma16816(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
         }
     }
 }
 
-__device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, int u, int lane,
-                                           Unit& U) {
+// Normalise O^T and stage it, transposed, in this warp's output buffer (rows
+// (query, head) of the pair, 128-byte swizzle) for the TMA store; the
+// log-sum-exp goes straight out.
+__device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, int u, int k, uint32_t obuf,
+                                           const Lane& L, int lane, Unit& U) {
     const int g8 = lane >> 2, tig = lane & 3;
     float l0 = U.l[0], l1 = U.l[1];
 #pragma unroll
@@ -544,23 +572,15 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
         l1 += __shfl_xor_sync(kFull, l1, w);
     }
     const float inv0 = 1.f / l0, inv1 = 1.f / l1;
-    // column g8 of the transposed fragments: query i0 + u + g8/4, head g*4 + g8%4
-    const int iq = x.i0 + u + (g8 >> 2);
-    const bool in = iq < P.a.T;
-    __nv_bfloat16* op = P.o + (((size_t)x.b * P.a.T + (in ? iq : 0)) * kHq + x.g * kG + (g8 & 3)) * kD +
-                        2 * tig;
+    const uint32_t buf = obuf + (uint32_t)(k * 8 * ROWB);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = movm_t(pack_bf16(U.o[j][0] * inv0, U.o[j][1] * inv1));
-        const uint32_t hi = movm_t(pack_bf16(U.o[j][2] * inv0, U.o[j][3] * inv1));
-        if (in) {
-            *reinterpret_cast<uint32_t*>(op + 16 * j) = lo;
-            *reinterpret_cast<uint32_t*>(op + 16 * j + 8) = hi;
-        }
-    }
+    for (int jj = 0; jj < 2; ++jj)
+        stsm_x4_t(buf + L.ob[jj], pack_bf16(U.o[2 * jj][0] * inv0, U.o[2 * jj][1] * inv1),
+                  pack_bf16(U.o[2 * jj][2] * inv0, U.o[2 * jj][3] * inv1),
+                  pack_bf16(U.o[2 * jj + 1][0] * inv0, U.o[2 * jj + 1][1] * inv1),
+                  pack_bf16(U.o[2 * jj + 1][2] * inv0, U.o[2 * jj + 1][3] * inv1));
     if (P.lse && g8 == 0) {
-        const int q = tig >> 1;
-        const int iq2 = x.i0 + u + q;
+        const int iq2 = x.i0 + u + (tig >> 1);
         if (iq2 < P.a.T) {
             const float2 v = make_float2((U.m[0] + __log2f(l0)) * kLn2, (U.m[1] + __log2f(l1)) * kLn2);
             *reinterpret_cast<float2*>(P.lse + ((size_t)x.b * P.a.T + iq2) * kHq + x.g * kG +
@@ -572,61 +592,70 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
 __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) {
     int wcount = 0, rcount = 0;
     const int u0 = 4 * warp;  // query pairs at tile offsets u0 and u0 + 2
-    const Lane L = make_lane(lane, P.a.W);
+    const Lane L = make_lane(lane, u0, P.a.W, P.win_rows);
+    const uint32_t obuf = S.obuf + (uint32_t)(warp * kObufBytes);
+    const int nr = max(P.a.nr, 1);
     uint32_t raw[2][4][2];
+    Tile x = decode(P, blockIdx.x);
     if (blockIdx.x < P.ntiles) {
-        const Tile x = decode(P, blockIdx.x);
 #pragma unroll
         for (int k = 0; k < 2; ++k) fetch_q(P, x, u0 + 2 * k, lane, raw[k]);
     }
     for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
-        const Tile x = decode(P, t);
         Unit U[2];
         int kt;
         {
-            const int slot = wcount % NWS;
-            bool ok = mbar_wait(bar_full_w(S, slot), (wcount / NWS) & 1, S.abort_flag);
-            if (!__all_sync(kFull, ok)) goto fail;
-            const uint32_t base = S.win + slot * P.win_slot_bytes;
+            if (!warp_wait(bar_full_w(S, 0), wcount & 1, S.abort_flag)) goto fail;
+            const uint32_t base = S.win;
+            const int nq = min(TQ, P.a.T - x.i0);
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
-                start_unit(P, base + 2 * P.win_region, x.i0, u0 + 2 * k, lane, raw[k], U[k]);
-            // the next tile's Q is in flight while this tile is computed
-            if (t + (int)gridDim.x < P.ntiles) {
-                const Tile nx = decode(P, t + gridDim.x);
-#pragma unroll
-                for (int k = 0; k < 2; ++k) fetch_q(P, nx, u0 + 2 * k, lane, raw[k]);
-            }
+            for (int k = 0; k < 2; ++k) start_unit(P, base + 2 * P.win_region, nq, u0 + 2 * k, lane, raw[k], U[k]);
             for (int wt = 0; wt < P.nwt; ++wt) window_tile(P, base, u0, x.i0, wt, L, U);
-            kt = S.kt[slot];
+            kt = S.kt[0];
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty_w(S, slot));
+            if (lane == 0) mbar_arrive(bar_empty_w(S, 0));
             ++wcount;
         }
-        {
-            for (int k0 = 0; k0 < kt; k0 += RUNGS_PER_TILE) {
-                const int np = min(RUNGS_PER_TILE, kt - k0);
-                bool ok = true;
-                for (int p = 0; p < np; ++p) {
-                    const int n = rcount + p;
-                    ok = ok && mbar_wait(bar_full_r(S, n % NRS), (n / NRS) & 1, S.abort_flag);
-                }
-                if (!__all_sync(kFull, ok)) goto fail;
-                rung_tiles(S, rcount, np, k0, u0, x.i0, L, U);
-                __syncwarp();
-                if (lane == 0)
-                    for (int p = 0; p < np; ++p) mbar_arrive(bar_empty_r(S, (rcount + p) % NRS));
-                rcount += np;
-            }
-        }
+        // the next tile's Q is in flight while this tile's rungs are computed
+        const Tile nx = decode(P, t + gridDim.x);
+        if (t + (int)gridDim.x < P.ntiles) {
 #pragma unroll
-        for (int k = 0; k < 2; ++k) store_unit(P, x, u0 + 2 * k, lane, U[k]);
+            for (int k = 0; k < 2; ++k) fetch_q(P, nx, u0 + 2 * k, lane, raw[k]);
+        }
+        for (int k0 = 0; k0 < kt; k0 += RUNGS_PER_TILE) {
+            const int np = min(RUNGS_PER_TILE, kt - k0);
+            for (int p = 0; p < np; ++p) {
+                const int n = rcount + p;
+                if (!warp_wait(bar_full_r(S, n & (NRS - 1)), (n / NRS) & 1, S.abort_flag)) goto fail;
+            }
+            rung_tiles(S, rcount, np, k0, nr, u0, x.i0, L, U);
+            __syncwarp();
+            if (lane < np) mbar_arrive(bar_empty_r(S, (rcount + lane) & (NRS - 1)));
+            rcount += np;
+        }
+        // the previous tile's stores must have read this warp's buffer
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) store_unit(P, x, u0 + 2 * k, k, obuf, L, lane, U[k]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if (x.i0 + u0 + 2 * k < P.a.T)
+                    tma_store_4d(&P.omap, obuf + (uint32_t)(k * 8 * ROWB), 0, x.g * kG, x.i0 + u0 + 2 * k, x.b);
+            bulk_commit();
+        }
+        x = nx;
     }
+    if (lane == 0) bulk_wait_all();
     return;
 fail:
     if (lane == 0) {
         *S.abort_flag = 1;
         if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
+        bulk_wait_all();
     }
 }
 
@@ -644,10 +673,13 @@ __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParam
     S.r = table;
     S.win = base + kHeaderBytes;
     S.rung = S.win + NWS * P.win_slot_bytes;
+    S.obuf = S.rung + NRS * kRungSlotBytes;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    S.tc = base + kTcOffset;
     if (threadIdx.x < P.a.nr) {
         const Rung rg = P.a.r[threadIdx.x];
         table[threadIdx.x] = SRung{rg.n, rg.t, rg.c};
+        reinterpret_cast<TC*>(hdr + kTcOffset)[threadIdx.x] = TC{rg.t, rg.c};
     }
     if (threadIdx.x == 0) {
         // full: one arrival (the producer's expect_tx) plus the copied bytes;
@@ -728,6 +760,20 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 4-D map over a [B][T][Hkv][64] bf16 tensor (innermost first: d, g, t, b),
 // box of `rows` rows of one head, 128-byte swizzle, zero fill outside.
+// 4-D map over O [B][T][8][64] bf16 (innermost first: d, head, t, b), box of
+// 2 queries x 4 heads, 128-byte swizzle (the staging buffer's layout).
+bool encode_out(CUtensorMap* m, void* base, int B, int T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHq, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kHq * kD * 2, (cuuint64_t)T * kHq * kD * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)kD, (cuuint32_t)kG, 2u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows(CUtensorMap* m, const void* base, int B, int T, int rows) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -787,12 +833,14 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) ||
         !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows))
         return cudaErrorInvalidValue;
+    if (!encode_out(&P.omap, o, a.B, a.T)) return cudaErrorInvalidValue;
     for (int p = 0; p < RUNGS_PER_TILE; ++p) {
         const int rows = RUNG_ROWS + ((3 * p) & 7);
         if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, rows) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, rows))
             return cudaErrorInvalidValue;
     }
-    const size_t smem = 1024 + kHeaderBytes + NWS * (size_t)P.win_slot_bytes + NRS * (size_t)kRungSlotBytes;
+    const size_t smem = 1024 + kHeaderBytes + NWS * (size_t)P.win_slot_bytes + NRS * (size_t)kRungSlotBytes +
+                        NCW * (size_t)kObufBytes;
     if (info.configured_smem < smem) {
         e = cudaFuncSetAttribute(fwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
