@@ -181,6 +181,23 @@ def sfa_forward(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE, rope_the
     return o, (lse if need_lse else None)
 
 
+def sfa_forward_noalloc(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
+                        rope_theta: float = 1e4, scale: float = 0.0, out, lse=None, rope=None,
+                        status=None, stream=None):
+    """sfa_forward without a workspace, for callers that cannot allocate device
+    memory: the scratch lives in a fixed array inside the library.  The caller
+    passes every buffer (``out``, ``lse`` and, when rope_theta > 0, a RoPE
+    table ``rope`` from sfa_rope_table); nothing is allocated here."""
+    _check_qkv(q, k, v)
+    B, T = q.shape[0], q.shape[1]
+    p = Params(B, T, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
+               dtype=q.dtype)
+    st = _lib.load().sfa_forward_noalloc(p.ref(), _vp(q), _vp(k), _vp(v), _vp(rope), _vp(out),
+                                         _vp(lse), _vp(status), _stream(q.device, stream))
+    _lib.check(st, "sfa_forward_noalloc")
+    return out, lse
+
+
 def sfa_backward_workspace_size(B: int, T: int, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
                                 dtype=torch.bfloat16) -> int:
     p = Params(B, T, W=W, alpha=alpha, rungs=rungs, dtype=dtype)

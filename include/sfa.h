@@ -163,6 +163,30 @@ SFA_API sfa_status sfa_forward(const sfa_params *p, const void *Q, const void *K
                                float *lse, void *workspace, size_t workspace_bytes,
                                unsigned int *status, cudaStream_t stream);
 
+/* ---- forward without a caller workspace ------------------------------- */
+
+/* The paper has no counterpart to this entry point: it serves callers that
+ * cannot allocate device memory (a plugin in a host application that owns all
+ * device memory, a fixed-footprint service, a tool limited to memory reserved
+ * up front).  It computes exactly what sfa_forward computes, with the same
+ * arguments minus the workspace: the bf16 path's rotated keys go to a fixed
+ * array inside the library, of sfa_forward_noalloc_scratch_bytes() bytes
+ * (8 MiB, enough for B * T <= 32768 tokens at Hkv = 2, D = 64), which every
+ * GPU that loads the library holds until the process exits.
+ *   - Returns SFA_ERR_UNSUPPORTED, before any launch, when the shape needs
+ *     more scratch than that; other errors as sfa_forward.
+ *   - Allocates nothing.  The first call on a device looks the array's device
+ *     address up (cudaGetSymbolAddress, with that device current) and caches
+ *     it; make that first call on each device before any stream capture.
+ *   - All calls share the one array: calls that overlap on the GPU (other
+ *     streams, other threads) race on it and give wrong results; order them
+ *     on one stream.  Nothing in the array needs to start at zero. */
+SFA_API size_t sfa_forward_noalloc_scratch_bytes(void);
+
+SFA_API sfa_status sfa_forward_noalloc(const sfa_params *p, const void *Q, const void *K,
+                                       const void *V, const float *rope_table, void *O,
+                                       float *lse, unsigned int *status, cudaStream_t stream);
+
 /* ---- backward ---------------------------------------------------------- */
 
 /* Bytes of device workspace sfa_backward needs for these parameters. */
