@@ -105,6 +105,17 @@ bool use_mma(const sfa_params* p, const LayerArgs& a) {
     return p->dtype == SFA_BF16 && sfa::fwd_mma_supported(a) && !force_simple;
 }
 
+// The bf16 backward runs on the tensor-core kernels for windows the forward
+// kernel also takes; SFA_BACKWARD_KERNEL=simple selects the fp32-arithmetic
+// kernel (read once), to compare the two on the same inputs.
+bool use_bwd_mma(const sfa_params* p, const LayerArgs& a) {
+    static const bool force_simple = [] {
+        const char* e = std::getenv("SFA_BACKWARD_KERNEL");
+        return e && std::strcmp(e, "simple") == 0;
+    }();
+    return p->dtype == SFA_BF16 && sfa::bwd_mma_supported(a) && !force_simple;
+}
+
 sfa_status launched(cudaError_t e) {
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
@@ -241,7 +252,7 @@ SFA_API size_t sfa_backward_workspace_size(const sfa_params* p) {
     if (validate(p) != SFA_OK) return 0;
     LayerArgs a;
     fill_args(p, &a);
-    return sfa::bwd_simple_workspace(a);
+    return use_bwd_mma(p, a) ? sfa::bwd_mma_workspace(a, p->rope_theta > 0.f) : sfa::bwd_simple_workspace(a);
 }
 
 SFA_API sfa_status sfa_backward(const sfa_params* p, const void* Q, const void* K, const void* V,
@@ -250,7 +261,6 @@ SFA_API sfa_status sfa_backward(const sfa_params* p, const void* Q, const void* 
                                 float* dalpha, float* dtheta, void* workspace,
                                 size_t workspace_bytes, unsigned int* status,
                                 cudaStream_t stream) {
-    (void)status;
     sfa_status st = validate(p);
     if (st != SFA_OK) return st;
     if (!dalpha || !dtheta || (reinterpret_cast<uintptr_t>(dalpha) & 3u) ||
@@ -269,9 +279,13 @@ SFA_API sfa_status sfa_backward(const sfa_params* p, const void* Q, const void* 
         if (!q || !aligned16(q)) return SFA_ERR_INVALID_ARG;
     if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
     if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
-    const size_t need = sfa::bwd_simple_workspace(a);
+    const bool mma = use_bwd_mma(p, a);
+    const size_t need = mma ? sfa::bwd_mma_workspace(a, p->rope_theta > 0.f) : sfa::bwd_simple_workspace(a);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
         return SFA_ERR_INVALID_ARG;
+    if (mma)
+        return launched(sfa::launch_bwd_mma(a, Q, K, V, O, dO, lse, rope_ptr(p, rope_table), dQ, dK, dV,
+                                            dalpha, dtheta, workspace, status, stream));
     return launched(sfa::launch_bwd_simple(a, p->dtype, Q, K, V, O, dO, lse, rope_ptr(p, rope_table),
                                            dQ, dK, dV, dalpha, dtheta, workspace, stream));
 }

@@ -1,0 +1,780 @@
+// sfa_bwd_mma.cu -- bf16 backward on the tensor cores (mma.sync, fp32
+// accumulation), the fast path of sfa_backward.
+//
+// Gradients of the attention of "Depth-Staggered Fibonacci Spacing for Sparse
+// Attention" (arXiv 2606.28560), section 2 "Attended set" and
+// "Implementation notes": for query i, head h and every entry e of its key
+// list (window rows, and per rung the interpolation of rows a = i - n (weight
+// 1 - t) and b = i - n - 1 (weight t)), with the forward's log-sum-exp and
+// D = dO . O,
+//   p = exp(s - lse), dp = dO . vtilde, ds = p (dp - D),
+//   dqhat += scale ds ktilde,  dkhat[row] += w scale ds qhat,  dv[row] += w p dO,
+//   dL/dt += scale ds (qhat . khat_b - qhat . khat_a) + p (dO . v_b - dO . v_a),
+// dL/dalpha = sum_k f_k dL/dt_k, dL/dtheta = dL/dalpha (alpha - 0.5)(1.5 - alpha).
+//
+// Three launches:
+//  1. bwd_prep_kernel: Khat = RoPE(K) (bf16, natural dimension order) into the
+//     workspace and zeroes the fp32 dKhat / dV accumulators.
+//  2. bwd_mma_kernel: persistent, the forward's tile map and load ring (one
+//     producer lane, seven consumer warps, a warp owns a quad of queries as
+//     two pairs).  Per M tile ("keys on M", as in the forward) it recomputes
+//     S^T = Khat_rows . Qhat^T and dP^T = V_rows . dO^T, forms p and ds, and
+//       dQhat^T += Khat_rows^T . dS^T        (registers, one tile at a time)
+//       dKhat_rows = dS . Qhat, dV_rows = P . dO   (m16n8k8 / m16n8k16)
+//     The interpolation weights split ds and p onto rows a and b inside the
+//     thread, exactly as in the forward.  Rows that several M rows of a warp
+//     share (row a of query i is row b of query i + 1) are summed in registers
+//     and the sums go to the fp32 accumulators with red.global.add.v2.  dQ is
+//     rotated back (R(i)^T) and stored through shared memory by TMA; dL/dt is
+//     summed per warp in shared memory and per CTA into the workspace.
+//  3. bwd_finish_kernel: dK = R(j)^T dKhat and dV to the caller's dtype, and
+//     the fixed-order (fp64) reduction of dL/dalpha and dL/dtheta.
+#include <cstring>
+
+#include "sfa_internal.cuh"
+#include "sfa_mma.cuh"
+#include "sfa_ring.cuh"
+
+namespace sfa {
+
+namespace {
+
+using namespace mma;
+using namespace ring;
+
+constexpr unsigned kObufBytes = 2 * 8 * ROWB;  // per consumer warp: dQ of 2 query pairs
+constexpr unsigned kDtBytes = NCW * SFA_MAX_RUNGS * 4;
+constexpr int kMaxGrid = 1024;                 // CTAs of the persistent kernel (dL/dt partials)
+constexpr int kPrepThreads = 256;
+constexpr int kFinishThreads = 256;
+
+struct BwdParams {
+    CUtensorMap kmap_w;
+    CUtensorMap vmap_w;
+    CUtensorMap kmap_r[RPG];
+    CUtensorMap vmap_r[RPG];
+    CUtensorMap dqmap;         // dQ [B][T][8][64], box of 2 queries x 4 heads
+    LayerArgs a;
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* o;
+    const __nv_bfloat16* dO;
+    const float* lse;
+    const float2* rope;        // nullptr: inputs are used as given
+    float* dk_acc;             // [B][T][Hkv][D] fp32, rotated frame
+    float* dv_acc;
+    float* dt_part;            // [gridDim.x][SFA_MAX_RUNGS]
+    unsigned* status;
+    float sl2;                 // scale x log2(e)
+    float scale;
+    int ntq, ntiles;
+    int step_g, step_tq, step_b;
+    int win_rows, nwt;
+    unsigned win_region, win_slot_bytes;
+};
+
+// ------------------------------------------------------------ consumers
+
+// One query pair of the warp's quad: B fragments of Qhat^T and dO^T in the
+// natural dimension order (k-step s, half h: dimensions 16 s + 8 h + 2 tig +
+// {0, 1} of column g8), the dQhat^T accumulators, and the per-column
+// constants of this thread's two C columns (query tig / 2, heads 2 (tig & 1)
+// + {0, 1}).
+struct BUnit {
+    uint32_t qf[4][2];
+    uint32_t df[4][2];
+    uint32_t qm[8];     // Qhat as the B operand of dKhat_rows (8-dimension chunk c)
+    uint32_t dm[8];     // dO as the B operand of dV_rows
+    float dq[4][4];
+    float2 lse2;        // log-sum-exp x log2(e)
+    float2 D;           // dO . O
+    bool qok;           // this thread's C-column query lies inside the sequence
+};
+
+struct BLane {
+    int g8, q;
+    bool useful;        // this thread's rung rows belong to its column query
+    bool is_a;          // lanes 0..15: query e = 0 of each pair
+    unsigned wmask;
+    uint32_t kn[2];     // rung tile of unit k: non-transposed row offsets (Khat; + kRungRegion: V)
+    uint32_t kt[2];     // rung tile of unit k: transposed row offsets (Khat)
+    uint32_t wk, wt;    // window tile 0: non-transposed / transposed row offsets
+    uint32_t ob[2];
+};
+
+__device__ __forceinline__ BLane make_blane(int lane, int u0, int W, int win_rows) {
+    BLane L;
+    L.g8 = lane >> 2;
+    L.q = (lane & 3) >> 1;
+    L.useful = (L.g8 >> 2) == L.q;
+    L.is_a = lane < 16;
+    const int p = lane & 3, e = (lane >> 2) & 1;
+    for (int k = 0; k < 2; ++k) {
+        const int u = u0 + 2 * k;
+        L.kn[k] = rung_row(p, u, e, (lane >> 3) & 1, lane >> 4, false);
+        L.kt[k] = rung_row(p, u, e, lane >> 4, (lane >> 3) & 1, false);
+    }
+    const int rk = (lane & 7) + (((lane >> 3) & 1) << 3);
+    const int rv = (lane & 7) + ((lane >> 4) << 3);
+    L.wk = swz_row(min(u0 + rk, win_rows - 1), lane >> 4);
+    L.wt = swz_row(min(u0 + rv, win_rows - 1), (lane >> 3) & 1);
+    L.wmask = 0u;
+    for (int wt = 0; wt < 3; ++wt)
+        for (int k = 0; k < 2; ++k)
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const int R = 16 * wt + L.g8 + ((e2 >> 1) << 3);
+                const int qq = 2 * k + L.q;
+                if (R >= qq && R <= W + qq) L.wmask |= 1u << (8 * wt + 4 * k + e2);
+            }
+    const int row = lane & 7, mi = lane >> 3;
+    for (int jj = 0; jj < 2; ++jj) {
+        const int chunk = 2 * (2 * jj + (mi >> 1)) + (mi & 1);
+        L.ob[jj] = (uint32_t)(row * ROWB) + (uint32_t)(((chunk ^ row) & 7) << 4);
+    }
+    return L;
+}
+
+__device__ __forceinline__ void red_v2(float* p, float a, float b) {
+    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+}
+
+// Adds (a, b) to acc[row][dim], dim even, unless the row lies outside the
+// sequence or the pair is zero.
+__device__ __forceinline__ void red_row(float* acc, size_t row_base, int row, int T, int dim, float2 v,
+                                        bool ok) {
+    if (ok && row >= 0 && row < T && (v.x != 0.f || v.y != 0.f))
+        red_v2(acc + (row_base + (size_t)row * kHkv) * kD + dim, v.x, v.y);
+}
+
+__device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 f2mul(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
+__device__ __forceinline__ float2 shfl2_xor(float2 v, int m) {
+    return f2(__shfl_xor_sync(kFull, v.x, m), __shfl_xor_sync(kFull, v.y, m));
+}
+
+// D = A (16 x 8 bf16, row) * B (8 x 8 bf16, col), fp32 (no accumulator input).
+__device__ __forceinline__ void mma1688_z(float d[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+        "{%7,%7,%7,%7};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0), "f"(0.0f));
+}
+
+// Loads the natural-order B-fragment words of one [.][8][64] bf16 row:
+// word (s, h) = dimensions 16 s + 8 h + 2 tig + {0, 1}.
+__device__ __forceinline__ void load_frag(const __nv_bfloat16* row, int tig, uint32_t w[4][2]) {
+    const unsigned* p = reinterpret_cast<const unsigned*>(row) + tig;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+        w[s][0] = __ldg(p + 8 * s);
+        w[s][1] = __ldg(p + 8 * s + 4);
+    }
+}
+
+// Start of a tile for unit k (query pair at tile offset u): Qhat^T, dO^T and
+// their dK/dV forms, D and the log-sum-exp of this thread's C columns.
+__device__ __forceinline__ void start_bunit(const BwdParams& P, const Tile& x, uint32_t tab, int nq, int u,
+                                            int lane, BUnit& U) {
+    const int g8 = lane >> 2, tig = lane & 3;
+    const int T = P.a.T;
+    // B-fragment column: query u + g8/4, head g8 % 4
+    const int iq = min(x.i0 + u + (g8 >> 2), T - 1);
+    const size_t rq = (((size_t)x.b * T + iq) * kHq + x.g * kG + (g8 & 3)) * kD;
+    uint32_t ow[4][2];
+    load_frag(P.q + rq, tig, U.qf);
+    load_frag(P.dO + rq, tig, U.df);
+    load_frag(P.o + rq, tig, ow);
+    // C columns: query u + tig/2, heads 2 (tig & 1) + {0, 1}
+    const int ic = x.i0 + u + (tig >> 1);
+    U.qok = ic < T;
+    const float* lp = P.lse + ((size_t)x.b * T + min(ic, T - 1)) * kHq + x.g * kG + 2 * (tig & 1);
+    U.lse2 = f2(__ldg(lp) * kLog2e, __ldg(lp + 1) * kLog2e);
+    // D of column g8 over this thread's 16 dimensions, then the quad of tig
+    float dpart = 0.f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float2 a = unpack_bf16(U.df[s][h]), b = unpack_bf16(ow[s][h]);
+            dpart = fmaf(a.x, b.x, fmaf(a.y, b.y, dpart));
+        }
+    dpart += __shfl_xor_sync(kFull, dpart, 1);
+    dpart += __shfl_xor_sync(kFull, dpart, 2);
+    U.D = f2(__shfl_sync(kFull, dpart, 4 * (2 * tig)), __shfl_sync(kFull, dpart, 4 * (2 * tig + 1)));
+    if (P.rope) {
+        // rotation pairs (m, m + 32): words (s, h) and (s + 2, h) of the thread
+        const uint32_t trow = tab + (uint32_t)(min(u + (g8 >> 2), nq - 1) * TABB);
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int m = 16 * s + 8 * h + 2 * tig;
+                const float4 cs = lds_f4(trow + (uint32_t)(m * 8));
+                const float2 xv = unpack_bf16(U.qf[s][h]), yv = unpack_bf16(U.qf[s + 2][h]);
+                U.qf[s][h] = pack_bf16(xv.x * cs.x - yv.x * cs.y, xv.y * cs.z - yv.y * cs.w);
+                U.qf[s + 2][h] = pack_bf16(yv.x * cs.x + xv.x * cs.y, yv.y * cs.z + xv.y * cs.w);
+            }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        U.qm[c] = movm_t(U.qf[c >> 1][c & 1]);
+        U.dm[c] = movm_t(U.df[c >> 1][c & 1]);
+    }
+}
+
+// Window M tile wt of the quad at tile offset u0 (rows u0 + 16 wt .. of the
+// window block, positions i0 + u0 - W + R).
+template <bool kFirst>
+__device__ __forceinline__ void bwd_window_tile(const BwdParams& P, uint32_t slot, const Tile& x, int u0, int wt,
+                                                const BLane& L, BUnit* U) {
+    const int lane = threadIdx.x & 31;
+    const int i0 = x.i0;
+    uint32_t kro = L.wk, tro = L.wt;
+    if (!kFirst) {
+        const int maxr = P.win_rows - 1;
+        kro = swz_row(min(u0 + 16 * wt + (lane & 7) + (((lane >> 3) & 1) << 3), maxr), lane >> 4);
+        tro = swz_row(min(u0 + 16 * wt + (lane & 7) + ((lane >> 4) << 3), maxr), (lane >> 3) & 1);
+    }
+    const uint32_t vslot = slot + P.win_region;
+    float cs[2][4], cp[2][4];
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+        uint32_t a0, a1, a2, a3, v0, v1, v2, v3;
+        ldsm_x4(slot + (kro ^ (uint32_t)(s2 << 5)), a0, a1, a2, a3);
+        ldsm_x4(vslot + (kro ^ (uint32_t)(s2 << 5)), v0, v1, v2, v3);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (s2 == 0) {
+                mma16816_z(cs[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+                mma16816_z(cp[k], v0, v1, v2, v3, U[k].df[s2][0], U[k].df[s2][1]);
+            } else {
+                mma16816(cs[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+                mma16816(cp[k], v0, v1, v2, v3, U[k].df[s2][0], U[k].df[s2][1]);
+            }
+        }
+    }
+    unsigned mask = L.wmask >> (8 * wt);
+    const int lo = P.a.W - (i0 + u0) - 16 * wt;
+    if (lo > 0) {
+        if (L.g8 < lo) mask &= ~0x33u;
+        if (L.g8 + 8 < lo) mask &= ~0xccu;
+    }
+    uint32_t bq[2][2], ad[2][2], ap[2][2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float pv[4], dsv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const bool ok = ((mask >> (4 * k + e)) & 1u) && U[k].qok;
+            const float l2 = (e & 1) ? U[k].lse2.y : U[k].lse2.x;
+            const float Dv = (e & 1) ? U[k].D.y : U[k].D.x;
+            const float pe = ok ? fast_exp2(fmaf(cs[k][e], P.sl2, -l2)) : 0.f;
+            pv[e] = pe;
+            dsv[e] = pe * (cp[k][e] - Dv) * P.scale;
+        }
+        ad[k][0] = pack_bf16(dsv[0], dsv[1]);
+        ad[k][1] = pack_bf16(dsv[2], dsv[3]);
+        ap[k][0] = pack_bf16(pv[0], pv[1]);
+        ap[k][1] = pack_bf16(pv[2], pv[3]);
+        bq[k][0] = movm_t(ad[k][0]);
+        bq[k][1] = movm_t(ad[k][1]);
+    }
+    // dQhat^T += Khat_rows^T . dS^T
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(slot + (tro ^ (uint32_t)(j << 5)), a0, a1, a2, a3);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (kFirst)
+                mma16816_z(U[k].dq[j], a0, a1, a2, a3, bq[k][0], bq[k][1]);
+            else
+                mma16816(U[k].dq[j], a0, a1, a2, a3, bq[k][0], bq[k][1]);
+        }
+    }
+    // dKhat_rows = dS . Qhat and dV_rows = P . dO over both pairs (k = 16
+    // columns), this thread's rows g8 and g8 + 8, dimensions 8 c + 2 tig + {0, 1}
+    const int tig = lane & 3;
+    const int r0 = i0 + u0 - P.a.W + 16 * wt + L.g8;
+    const bool use0 = 16 * wt + L.g8 <= P.a.W + 3, use1 = 16 * wt + L.g8 + 8 <= P.a.W + 3;
+    const size_t rb = (size_t)x.b * P.a.T * kHkv + x.g;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        float dk[4], dv[4];
+        mma16816_z(dk, ad[0][0], ad[0][1], ad[1][0], ad[1][1], U[0].qm[c], U[1].qm[c]);
+        mma16816_z(dv, ap[0][0], ap[0][1], ap[1][0], ap[1][1], U[0].dm[c], U[1].dm[c]);
+        const int dim = 8 * c + 2 * tig;
+        red_row(P.dk_acc, rb, r0, P.a.T, dim, f2(dk[0], dk[1]), use0);
+        red_row(P.dk_acc, rb, r0 + 8, P.a.T, dim, f2(dk[2], dk[3]), use1);
+        red_row(P.dv_acc, rb, r0, P.a.T, dim, f2(dv[0], dv[1]), use0);
+        red_row(P.dv_acc, rb, r0 + 8, P.a.T, dim, f2(dv[2], dv[3]), use1);
+    }
+}
+
+// Rung M tiles of the quad (pairs at tile offsets u0, u0 + 2) for the np
+// rungs k0 .. k0 + np - 1 of the group in slot gslot.
+__device__ __forceinline__ void bwd_rung_tile(const BwdParams& P, const Smem& S, uint32_t gslot, const Tile& x,
+                                              int k0, int np, int nr, int u0, const BLane& L, BUnit* U,
+                                              float* dt_w) {
+    const int lane = threadIdx.x & 31;
+    const int tig = lane & 3;
+    uint32_t kn[2], kt[2];
+    if (np == RPG) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            kn[k] = gslot + L.kn[k];
+            kt[k] = gslot + L.kt[k];
+        }
+    } else {
+        const int p = (lane & 3) < np ? (lane & 3) : 0, e = (lane >> 2) & 1;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            kn[k] = gslot + rung_row(p, u0 + 2 * k, e, (lane >> 3) & 1, lane >> 4, false);
+            kt[k] = gslot + rung_row(p, u0 + 2 * k, e, lane >> 4, (lane >> 3) & 1, false);
+        }
+    }
+    // S^T = Khat_rows . Qhat^T, dP^T = V_rows . dO^T
+    float cs[2][4], cp[2][4];
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t a0, a1, a2, a3, v0, v1, v2, v3;
+            ldsm_x4(kn[k] ^ (uint32_t)(s2 << 5), a0, a1, a2, a3);
+            ldsm_x4((kn[k] + kRungRegion) ^ (uint32_t)(s2 << 5), v0, v1, v2, v3);
+            if (s2 == 0) {
+                mma16816_z(cs[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+                mma16816_z(cp[k], v0, v1, v2, v3, U[k].df[s2][0], U[k].df[s2][1]);
+            } else {
+                mma16816(cs[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+                mma16816(cp[k], v0, v1, v2, v3, U[k].df[s2][0], U[k].df[s2][1]);
+            }
+        }
+    }
+    // rows b (c0, c1) and a (c2, c3) of rung k0 + p for query q of each pair
+    const int p = L.g8 & 3;
+    const TC tc = lds_tc(S.tc + (uint32_t)(min(k0 + p, nr - 1) * 8));
+    const bool rung_ok = L.useful && p < np;
+    const float t = tc.t, omt = 1.f - tc.t;
+    uint32_t bq[2][2], ad[2][2], ap[2][2];
+    float dt = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int i = x.i0 + u0 + 2 * k + L.q;
+        const bool ok = rung_ok && U[k].qok && i >= tc.c;
+        const float2 sb = f2(cs[k][0], cs[k][1]), sa = f2(cs[k][2], cs[k][3]);
+        const float2 db = f2(cp[k][0], cp[k][1]), da = f2(cp[k][2], cp[k][3]);
+        const float2 sv = __ffma2_rn(f2(t, t), sb, f2mul(f2(omt, omt), sa));
+        const float2 dpv = __ffma2_rn(f2(t, t), db, f2mul(f2(omt, omt), da));
+        const float2 pe = ok ? f2(fast_exp2(fmaf(sv.x, P.sl2, -U[k].lse2.x)),
+                                  fast_exp2(fmaf(sv.y, P.sl2, -U[k].lse2.y)))
+                             : f2(0.f, 0.f);
+        const float2 ds = f2mul(f2mul(pe, f2(dpv.x - U[k].D.x, dpv.y - U[k].D.y)), f2(P.scale, P.scale));
+        // dL/dt: ds (s_b - s_a) (raw scores, scale folded into ds) + p (dp_b - dp_a);
+        // at t = 0 the derivative is one-sided and zero while row b = i - n - 1
+        // lies before the sequence start (i = ceil(d) = n)
+        const float2 g = __ffma2_rn(ds, f2(sb.x - sa.x, sb.y - sa.y), f2mul(pe, f2(db.x - da.x, db.y - da.y)));
+        if (t > 0.f || i > tc.c) dt += g.x + g.y;
+        ad[k][0] = pack_bf16(ds.x * t, ds.y * t);        // row b
+        ad[k][1] = pack_bf16(ds.x * omt, ds.y * omt);    // row a
+        ap[k][0] = pack_bf16(pe.x * t, pe.y * t);
+        ap[k][1] = pack_bf16(pe.x * omt, pe.y * omt);
+        bq[k][0] = movm_t(ad[k][0]);
+        bq[k][1] = movm_t(ad[k][1]);
+    }
+    // dL/dt of rung k0 + p: the threads g8 in {p, p + 4}, every tig
+    dt += __shfl_xor_sync(kFull, dt, 1);
+    dt += __shfl_xor_sync(kFull, dt, 2);
+    dt += __shfl_xor_sync(kFull, dt, 16);
+    if (lane < 16 && tig == 0 && p < np) dt_w[k0 + p] += dt;
+    // dQhat^T += Khat_rows^T . dS^T
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(kt[k] ^ (uint32_t)(j << 5), a0, a1, a2, a3);
+            mma16816(U[k].dq[j], a0, a1, a2, a3, bq[k][0], bq[k][1]);
+        }
+    }
+    // dKhat_rows = dS . Qhat, dV_rows = P . dO.  Rows base + m, m = 2k + e +
+    // kind: lanes 0..15 (e = 0) hold m = 0, 1 (pair 0) and 2, 3 (pair 1),
+    // lanes 16..31 hold m = 1, 2 and 3, 4; the shared rows are summed across
+    // the two halves of the warp before the reduction.
+    const int base = x.i0 + u0 - S.r[min(k0 + p, nr - 1)].n - 1;
+    const bool pok = p < np;
+    const size_t rb = (size_t)x.b * P.a.T * kHkv + x.g;
+    const bool A = L.is_a;
+#pragma unroll
+    for (int tensor = 0; tensor < 2; ++tensor) {
+        float* acc = tensor == 0 ? P.dk_acc : P.dv_acc;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float m0[4], m1[4];
+            if (tensor == 0) {
+                mma1688_z(m0, ad[0][0], ad[0][1], U[0].qm[c]);
+                mma1688_z(m1, ad[1][0], ad[1][1], U[1].qm[c]);
+            } else {
+                mma1688_z(m0, ap[0][0], ap[0][1], U[0].dm[c]);
+                mma1688_z(m1, ap[1][0], ap[1][1], U[1].dm[c]);
+            }
+            const float2 u0b = f2(m0[0], m0[1]), u0a = f2(m0[2], m0[3]);
+            const float2 u1b = f2(m1[0], m1[1]), u1a = f2(m1[2], m1[3]);
+            const float2 r1 = shfl2_xor(A ? u1a : u0b, 16);
+            const float2 r2 = shfl2_xor(u0a, 16);
+            const int dim = 8 * c + 2 * tig;
+            red_row(acc, rb, base + (A ? 0 : 3), P.a.T, dim, A ? u0b : f2add(u1b, r1), pok);
+            red_row(acc, rb, base + (A ? 1 : 4), P.a.T, dim, A ? f2add(u0a, r1) : u1a, pok);
+            red_row(acc, rb, base + 2, P.a.T, dim, f2add(u1b, r2), pok && A);
+        }
+    }
+}
+
+// dQ = R(i)^T dQhat of unit k, staged transposed in this warp's buffer for
+// the TMA store.
+__device__ __forceinline__ void store_dq(const BwdParams& P, const Tile& x, int u, int k, uint32_t obuf,
+                                         const BLane& L, int lane, BUnit& U) {
+    const int g8 = lane >> 2, tig = lane & 3;
+    if (P.rope) {
+        const int iq = min(x.i0 + u + (tig >> 1), P.a.T - 1);
+        const float2* tr = P.rope + (size_t)iq * kPairs;
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                // dimensions m = 16 j + 8 h + g8 (element 2 h, 2 h + 1) and m + 32 (m tile j + 2)
+                const float2 cs = __ldg(tr + 16 * j + 8 * h + g8);
+                const float x0 = U.dq[j][2 * h], x1 = U.dq[j][2 * h + 1];
+                const float y0 = U.dq[j + 2][2 * h], y1 = U.dq[j + 2][2 * h + 1];
+                U.dq[j][2 * h] = cs.x * x0 + cs.y * y0;
+                U.dq[j][2 * h + 1] = cs.x * x1 + cs.y * y1;
+                U.dq[j + 2][2 * h] = cs.x * y0 - cs.y * x0;
+                U.dq[j + 2][2 * h + 1] = cs.x * y1 - cs.y * x1;
+            }
+    }
+    const uint32_t buf = obuf + (uint32_t)(k * 8 * ROWB);
+    uint32_t r[4][2];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        r[j][0] = pack_bf16(U.dq[j][0], U.dq[j][1]);
+        r[j][1] = pack_bf16(U.dq[j][2], U.dq[j][3]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < 2; ++jj)
+        stsm_x4_t(buf + L.ob[jj], r[2 * jj][0], r[2 * jj][1], r[2 * jj + 1][0], r[2 * jj + 1][1]);
+}
+
+__device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int lane, float* dt_w) {
+    int wcount = 0, gcount = 0;
+    const int u0 = 4 * warp;
+    const BLane L = make_blane(lane, u0, P.a.W, P.win_rows);
+    const uint32_t obuf = S.obuf + (uint32_t)(warp * kObufBytes);
+    const int nr = max(P.a.nr, 1);
+    // the accumulators are zeroed by the launch before this one
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    Tile x = decode(P, blockIdx.x);
+    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
+        BUnit U[2];
+        int kt;
+        {
+            if (!warp_wait(bar_full_w(S), wcount & 1, S.abort_flag)) goto fail;
+            const int nq = min(TQ, P.a.T - x.i0);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) start_bunit(P, x, S.win + 2 * P.win_region, nq, u0 + 2 * k, lane, U[k]);
+            bwd_window_tile<true>(P, S.win, x, u0, 0, L, U);
+            for (int wt = 1; wt < P.nwt; ++wt) bwd_window_tile<false>(P, S.win, x, u0, wt, L, U);
+            kt = *S.kt;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty_w(S));
+            ++wcount;
+        }
+        for (int k0 = 0; k0 < kt; k0 += RPG) {
+            const int slot = gcount & (NGS - 1);
+            if (!warp_wait(bar_full_g(S, slot), (gcount / NGS) & 1, S.abort_flag)) goto fail;
+            bwd_rung_tile(P, S, S.rung + (uint32_t)slot * kGroupSlotBytes, x, k0, min(RPG, kt - k0), nr, u0, L,
+                          U, dt_w);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty_g(S, slot));
+            ++gcount;
+        }
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k) store_dq(P, x, u0 + 2 * k, k, obuf, L, lane, U[k]);
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k)
+                if (x.i0 + u0 + 2 * k < P.a.T)
+                    tma_store_4d(&P.dqmap, obuf + (uint32_t)(k * 8 * ROWB), 0, x.g * kG, x.i0 + u0 + 2 * k, x.b);
+            bulk_commit();
+        }
+        x = next_tile(P, x);
+    }
+    if (lane == 0) bulk_wait_all();
+    return;
+fail:
+    if (lane == 0) {
+        *S.abort_flag = 1;
+        if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
+        bulk_wait_all();
+    }
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_constant__ BwdParams P) {
+    extern __shared__ unsigned char smem_raw[];
+    const Smem S = ring_setup(P.a, P.win_slot_bytes, smem_raw);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // per consumer warp dL/dt sums, after the output staging buffers
+    float* dt_all = reinterpret_cast<float*>(smem_raw + (S.obuf + NCW * kObufBytes - smem_u32(smem_raw)));
+    for (int i = threadIdx.x; i < NCW * SFA_MAX_RUNGS; i += blockDim.x) dt_all[i] = 0.f;
+    __syncthreads();
+    if (warp == NCW) {
+        if (lane == 0) producer(P, S);
+    } else {
+        bwd_consumer(P, S, warp, lane, dt_all + warp * SFA_MAX_RUNGS);
+    }
+    __syncthreads();
+    if (threadIdx.x < SFA_MAX_RUNGS) {
+        float s = 0.f;
+        for (int w = 0; w < NCW; ++w) s += dt_all[w * SFA_MAX_RUNGS + threadIdx.x];
+        P.dt_part[(size_t)blockIdx.x * SFA_MAX_RUNGS + threadIdx.x] = s;
+    }
+}
+
+// ------------------------------------------------------ prep and finish
+
+// Khat = RoPE(K) in the natural dimension order (skipped without a table) and
+// zero dKhat / dV accumulators.  Four threads per row (b, j, g): thread a
+// takes the rotation pairs 8a .. 8a + 7.
+__global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloat16* __restrict__ k,
+                                                                const float2* __restrict__ rope,
+                                                                __nv_bfloat16* __restrict__ khat,
+                                                                float* __restrict__ dk_acc,
+                                                                float* __restrict__ dv_acc, unsigned rows,
+                                                                unsigned T) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const unsigned idx = blockIdx.x * kPrepThreads + threadIdx.x;
+    const unsigned row = idx >> 2, a = idx & 3;
+    if (row >= rows) return;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4* dk4 = reinterpret_cast<float4*>(dk_acc + (size_t)row * kD + 16 * a);
+    float4* dv4 = reinterpret_cast<float4*>(dv_acc + (size_t)row * kD + 16 * a);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        dk4[i] = z;
+        dv4[i] = z;
+    }
+    if (!rope) return;
+    const unsigned j = (row / kHkv) % T;
+    const __nv_bfloat16* kr = k + (size_t)row * kD;
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(kr + 8 * a));
+    const uint4 yv = __ldg(reinterpret_cast<const uint4*>(kr + 32 + 8 * a));
+    const float4* cs = reinterpret_cast<const float4*>(rope + (size_t)j * kPairs + 8 * a);
+    uint32_t xo[4], yo[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const float4 t = __ldg(cs + c);
+        const float2 x = unpack_bf16(u4_get(xv, c));
+        const float2 y = unpack_bf16(u4_get(yv, c));
+        xo[c] = pack_bf16(x.x * t.x - y.x * t.y, x.y * t.z - y.y * t.w);
+        yo[c] = pack_bf16(y.x * t.x + x.x * t.y, y.y * t.z + x.y * t.w);
+    }
+    __nv_bfloat16* out = khat + (size_t)row * kD;
+    *reinterpret_cast<uint4*>(out + 8 * a) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+    *reinterpret_cast<uint4*>(out + 32 + 8 * a) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+}
+
+// dK = R(j)^T dKhat and dV, bf16, four threads per row (pairs 8a .. 8a + 7);
+// the last block reduces dL/dt over the CTA partials in a fixed order.
+__global__ void __launch_bounds__(kFinishThreads) bwd_finish_mma_kernel(
+    const LayerArgs a, const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
+    const float2* __restrict__ rope, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+    const float* __restrict__ dt_part, int nparts, float* __restrict__ dalpha, float* __restrict__ dtheta,
+    unsigned rows, unsigned row_blocks) {
+    if (blockIdx.x == row_blocks) {
+        __shared__ double red[kFinishThreads];
+        double total = 0.0;
+        for (int r = 0; r < a.nr; ++r) {
+            double s = 0.0;
+            for (int p = threadIdx.x; p < nparts; p += kFinishThreads)
+                s += (double)dt_part[(size_t)p * SFA_MAX_RUNGS + r];
+            red[threadIdx.x] = s;
+            __syncthreads();
+            for (int w = kFinishThreads / 2; w > 0; w >>= 1) {
+                if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+                __syncthreads();
+            }
+            if (threadIdx.x == 0) total += (double)a.r[r].f * red[0];
+            __syncthreads();
+        }
+        if (threadIdx.x == 0) {
+            const double al = (double)a.alpha;
+            *dalpha = (float)total;
+            *dtheta = (float)(total * (al - 0.5) * (1.5 - al));
+        }
+        return;
+    }
+    const unsigned idx = blockIdx.x * kFinishThreads + threadIdx.x;
+    const unsigned row = idx >> 2, q = idx & 3;
+    if (row >= rows) return;
+    const float4* xk = reinterpret_cast<const float4*>(dk_acc + (size_t)row * kD + 8 * q);
+    const float4* yk = reinterpret_cast<const float4*>(dk_acc + (size_t)row * kD + 32 + 8 * q);
+    const float4* xv = reinterpret_cast<const float4*>(dv_acc + (size_t)row * kD + 8 * q);
+    const float4* yv = reinterpret_cast<const float4*>(dv_acc + (size_t)row * kD + 32 + 8 * q);
+    float x[8], y[8];
+    *reinterpret_cast<float4*>(x) = xk[0];
+    *reinterpret_cast<float4*>(x + 4) = xk[1];
+    *reinterpret_cast<float4*>(y) = yk[0];
+    *reinterpret_cast<float4*>(y + 4) = yk[1];
+    if (rope) {
+        const unsigned j = (row / kHkv) % (unsigned)a.T;
+        const float4* cs = reinterpret_cast<const float4*>(rope + (size_t)j * kPairs + 8 * q);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const float4 t = __ldg(cs + c);
+            const float x0 = x[2 * c], x1 = x[2 * c + 1], y0 = y[2 * c], y1 = y[2 * c + 1];
+            x[2 * c] = t.x * x0 + t.y * y0;
+            y[2 * c] = t.x * y0 - t.y * x0;
+            x[2 * c + 1] = t.z * x1 + t.w * y1;
+            y[2 * c + 1] = t.z * y1 - t.w * x1;
+        }
+    }
+    uint4 ko0, ko1, vo0, vo1;
+    ko0 = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+    ko1 = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
+    const float4 v0 = xv[0], v1 = xv[1], v2 = yv[0], v3 = yv[1];
+    vo0 = make_uint4(pack_bf16(v0.x, v0.y), pack_bf16(v0.z, v0.w), pack_bf16(v1.x, v1.y), pack_bf16(v1.z, v1.w));
+    vo1 = make_uint4(pack_bf16(v2.x, v2.y), pack_bf16(v2.z, v2.w), pack_bf16(v3.x, v3.y), pack_bf16(v3.z, v3.w));
+    *reinterpret_cast<uint4*>(dk + (size_t)row * kD + 8 * q) = ko0;
+    *reinterpret_cast<uint4*>(dk + (size_t)row * kD + 32 + 8 * q) = ko1;
+    *reinterpret_cast<uint4*>(dv + (size_t)row * kD + 8 * q) = vo0;
+    *reinterpret_cast<uint4*>(dv + (size_t)row * kD + 32 + 8 * q) = vo1;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct BwdWorkspace {
+    __nv_bfloat16* khat;  // only with RoPE
+    float* dk_acc;
+    float* dv_acc;
+    float* dt_part;
+};
+
+BwdWorkspace carve(const LayerArgs& a, bool rope, void* base) {
+    const size_t nkv = (size_t)a.B * a.T * kHkv * kD;
+    char* p = static_cast<char*>(base);
+    BwdWorkspace w;
+    w.khat = nullptr;
+    if (rope) {
+        w.khat = reinterpret_cast<__nv_bfloat16*>(p);
+        p += align256(nkv * sizeof(__nv_bfloat16));
+    }
+    w.dk_acc = reinterpret_cast<float*>(p);
+    p += align256(nkv * sizeof(float));
+    w.dv_acc = reinterpret_cast<float*>(p);
+    p += align256(nkv * sizeof(float));
+    w.dt_part = reinterpret_cast<float*>(p);
+    return w;
+}
+
+}  // namespace
+
+bool bwd_mma_supported(const LayerArgs& a) { return a.W <= 30; }
+
+size_t bwd_mma_workspace(const LayerArgs& a, bool rope) {
+    const size_t nkv = (size_t)a.B * a.T * kHkv * kD;
+    return (rope ? align256(nkv * sizeof(__nv_bfloat16)) : 0) + 2 * align256(nkv * sizeof(float)) +
+           align256((size_t)kMaxGrid * SFA_MAX_RUNGS * sizeof(float));
+}
+
+cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, const float2* rope, void* dq, void* dk, void* dv,
+                           float* dalpha, float* dtheta, void* ws, unsigned* status, cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const int sms = sm_count(dev, &e);
+    if (e != cudaSuccess) return e;
+    const BwdWorkspace w = carve(a, rope != nullptr, ws);
+    const unsigned rows = (unsigned)a.B * (unsigned)a.T * kHkv;
+    {
+        const unsigned blocks = (rows * 4 + kPrepThreads - 1) / kPrepThreads;
+        bwd_prep_kernel<<<blocks, kPrepThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k), rope, w.khat,
+                                                        w.dk_acc, w.dv_acc, rows, (unsigned)a.T);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        count_launch();
+    }
+    const void* khat = rope ? static_cast<const void*>(w.khat) : k;
+    BwdParams P;
+    std::memset(&P, 0, sizeof(P));
+    P.a = a;
+    P.q = static_cast<const __nv_bfloat16*>(q);
+    P.o = static_cast<const __nv_bfloat16*>(o);
+    P.dO = static_cast<const __nv_bfloat16*>(dO);
+    P.lse = lse;
+    P.rope = rope;
+    P.dk_acc = w.dk_acc;
+    P.dv_acc = w.dv_acc;
+    P.dt_part = w.dt_part;
+    P.status = status;
+    P.sl2 = a.scale * kLog2e;
+    P.scale = a.scale;
+    P.ntq = (a.T + TQ - 1) / TQ;
+    P.ntiles = a.B * P.ntq * kHkv;
+    P.win_rows = TQ + a.W;
+    P.nwt = (a.W + 4 + 15) / 16;
+    P.win_region = round1k((unsigned)P.win_rows * ROWB);
+    P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
+    if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) || !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows) ||
+        !encode_out(&P.dqmap, dq, a.B, a.T))
+        return cudaErrorInvalidValue;
+    for (int p = 0; p < RPG; ++p) {
+        const int r = RUNG_ROWS + 2 * p;
+        if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, r) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, r))
+            return cudaErrorInvalidValue;
+    }
+    const size_t smem = 1024 + kHeaderBytes + (size_t)P.win_slot_bytes + NGS * (size_t)kGroupSlotBytes +
+                        NCW * (size_t)kObufBytes + kDtBytes;
+    static size_t configured_smem[64];
+    if (configured_smem[dev & 63] < smem) {
+        e = cudaFuncSetAttribute(bwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_smem[dev & 63] = smem;
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bwd_mma_kernel, NTHREADS, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    long long grid = (long long)sms * per_sm;
+    if (grid > P.ntiles) grid = P.ntiles;
+    if (grid > kMaxGrid) grid = kMaxGrid;
+    P.step_g = (int)(grid % kHkv);
+    P.step_tq = (int)((grid / kHkv) % P.ntq);
+    P.step_b = (int)((grid / kHkv) / P.ntq);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(NTHREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bwd_mma_kernel, P);
+    if (e != cudaSuccess) return e;
+    count_launch();
+    {
+        const unsigned row_blocks = (rows * 4 + kFinishThreads - 1) / kFinishThreads;
+        bwd_finish_mma_kernel<<<row_blocks + 1, kFinishThreads, 0, s>>>(
+            a, w.dk_acc, w.dv_acc, rope, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+            w.dt_part, (int)grid, dalpha, dtheta, rows, row_blocks);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        count_launch();
+    }
+    return cudaSuccess;
+}
+
+}  // namespace sfa

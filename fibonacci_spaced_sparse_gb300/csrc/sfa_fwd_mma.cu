@@ -48,33 +48,17 @@
 
 #include "sfa_internal.cuh"
 #include "sfa_mma.cuh"
+#include "sfa_ring.cuh"
 
 namespace sfa {
 
 namespace {
 
 using namespace mma;
+using namespace ring;
 
-constexpr int TQ = 28;                 // queries per tile
-constexpr int NCW = 7;                 // consumer warps (2 query pairs each)
-constexpr int NTHREADS = (NCW + 1) * 32;
-constexpr int RPG = 4;                 // rungs per group (one M tile of a query pair)
-constexpr int NGS = 2;                 // group slots
-constexpr int RUNG_ROWS = TQ + 1;      // rows a rung block needs
-constexpr int RUNG_BOX = RUNG_ROWS + 2 * (RPG - 1);
-constexpr int ROWB = 128;              // bytes of one 64-element bf16 row
-constexpr int TABB = kPairs * 8;       // bytes of one RoPE table row (32 x (cos, sin))
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLazy = 8.0f;          // raise the running max past this margin
 constexpr float kMinMax = -1e30f;      // floor of the running max (no entry yet)
-constexpr int kNoRung = 1 << 30;       // ceiling of a rung no query of the tile uses
-
-constexpr unsigned round1k(unsigned x) { return (x + 1023u) & ~1023u; }
-constexpr unsigned kRungRegion = round1k(RUNG_BOX * ROWB);  // one tensor of one rung
-constexpr unsigned kRungBytes = 2 * kRungRegion;            // Khat region, then V region
-constexpr unsigned kGroupSlotBytes = RPG * kRungBytes;
-constexpr unsigned kHeaderBytes = 1024;                     // barriers, flag, rung table
 constexpr unsigned kObufBytes = 2 * 8 * ROWB;               // per consumer warp: O of 2 query pairs
 
 struct FwdParams {
@@ -113,190 +97,7 @@ __host__ __device__ constexpr int kdim_of(int c, int tig, int j) {
     return c < 4 ? 8 * tig + 2 * c + j : 32 + 8 * tig + 2 * (c - 4) + j;
 }
 
-// -------------------------------------------------------------- tile map
-
-// Tile t = (b * ntq + tq) * Hkv + g covers queries i0 = tq * TQ .. of
-// sequence b, key/value head g.  A CTA takes tiles blockIdx.x, + gridDim.x, ...
-struct Tile {
-    int b, g, tq, i0;
-};
-
-__device__ __forceinline__ Tile decode(const FwdParams& P, int t) {
-    Tile x;
-    x.g = t % kHkv;
-    const int rest = t / kHkv;
-    x.tq = rest % P.ntq;
-    x.b = rest / P.ntq;
-    x.i0 = x.tq * TQ;
-    return x;
-}
-
-// The tile gridDim.x further on.
-__device__ __forceinline__ Tile next_tile(const FwdParams& P, const Tile& x) {
-    Tile y;
-    y.g = x.g + P.step_g;
-    const int cg = y.g >= kHkv;
-    y.g -= cg ? kHkv : 0;
-    y.tq = x.tq + P.step_tq + cg;
-    const int ct = y.tq >= P.ntq;
-    y.tq -= ct ? P.ntq : 0;
-    y.b = x.b + P.step_b + ct;
-    y.i0 = y.tq * TQ;
-    return y;
-}
-
-// ---------------------------------------------------------- smem layout
-
-struct SRung {
-    int n;
-    float t;
-    int c;
-};
-
-struct TC {
-    float t;
-    int c;
-};
-
-struct Smem {
-    uint32_t bars;      // full_w, empty_w, full_g[NGS], empty_g[NGS]
-    uint32_t win;       // the window slot
-    uint32_t rung;      // NGS group slots
-    uint32_t obuf;      // NCW output staging buffers
-    int* abort_flag;
-    int* kt;            // rungs usable by the window slot's tile
-    const SRung* r;     // the kept rungs, by increasing distance
-    uint32_t tc;        // shared address of TC[nr] (t and ceil of each kept rung)
-};
-
-__device__ __forceinline__ uint32_t bar_full_w(const Smem& s) { return s.bars; }
-__device__ __forceinline__ uint32_t bar_empty_w(const Smem& s) { return s.bars + 8; }
-__device__ __forceinline__ uint32_t bar_full_g(const Smem& s, int i) { return s.bars + 16 + 8 * i; }
-__device__ __forceinline__ uint32_t bar_empty_g(const Smem& s, int i) { return s.bars + 16 + 8 * (NGS + i); }
-constexpr int kBarBytes = 16 + 16 * NGS;
-constexpr int kFlagOffset = kBarBytes;
-constexpr int kKtOffset = kFlagOffset + 4;
-constexpr int kRungTableOffset = 256;
-constexpr int kTcOffset = kRungTableOffset + SFA_MAX_RUNGS * 12;  // {t, ceil} per rung, 8 bytes
-static_assert(kKtOffset + 4 <= kRungTableOffset, "header overflow");
-static_assert(kTcOffset + SFA_MAX_RUNGS * 8 <= (int)kHeaderBytes, "header overflow");
-
-// Rungs are sorted by ceil(d): those usable by some query of the tile form a prefix.
-__device__ __forceinline__ int active_rungs(const Smem& S, int nr, int i0) {
-    int n = 0;
-    while (n < nr && S.r[n].c <= i0 + TQ - 1) ++n;
-    return n;
-}
-
-// ------------------------------------------------------------ producer
-
-// Window block of tile x (and its RoPE rows) into the window slot; returns
-// the number of rungs the tile uses (published to the consumers in S.kt).
-__device__ __forceinline__ bool load_window(const FwdParams& P, const Smem& S, const Tile& x, int& wcount,
-                                            int& kt) {
-    if (!mbar_wait(bar_empty_w(S), (wcount & 1) ^ 1, S.abort_flag)) return false;
-    const int nq = min(TQ, P.a.T - x.i0);
-    const uint32_t tab_bytes = P.rope ? (uint32_t)nq * TABB : 0u;
-    kt = active_rungs(S, P.a.nr, x.i0);
-    *S.kt = kt;  // published by the arrive below
-    const uint32_t full = bar_full_w(S);
-    mbar_arrive_expect_tx(full, 2u * P.win_rows * ROWB + tab_bytes);
-    tma_load_4d(S.win, &P.kmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
-    tma_load_4d(S.win + P.win_region, &P.vmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
-    // RoPE rows of the tile's query positions (read by the consumers' Q rotation)
-    if (P.rope) bulk_g2s(S.win + 2 * P.win_region, P.rope + (size_t)x.i0 * kPairs, tab_bytes, full);
-    ++wcount;
-    return true;
-}
-
-// Rung group k0 .. k0 + 3 of tile x into the next group slot.
-__device__ __forceinline__ bool load_group(const FwdParams& P, const Smem& S, const Tile& x, int k0, int kt,
-                                           int& gcount) {
-    const int slot = gcount & (NGS - 1);
-    if (!mbar_wait(bar_empty_g(S, slot), ((gcount / NGS) & 1) ^ 1, S.abort_flag)) return false;
-    const int np = min(RPG, kt - k0);
-    const uint32_t base = S.rung + slot * kGroupSlotBytes;
-    const uint32_t full = bar_full_g(S, slot);
-    uint32_t bytes = 0;
-    for (int p = 0; p < np; ++p) bytes += 2u * (RUNG_ROWS + 2 * p) * ROWB;
-    mbar_arrive_expect_tx(full, bytes);
-    for (int p = 0; p < np; ++p) {
-        const int row0 = x.i0 - S.r[k0 + p].n - 1 - 2 * p;
-        const uint32_t dst = base + p * kRungBytes;
-        tma_load_4d(dst, &P.kmap_r[p], 0, x.g, row0, x.b, full);
-        tma_load_4d(dst + kRungRegion, &P.vmap_r[p], 0, x.g, row0, x.b, full);
-    }
-    ++gcount;
-    return true;
-}
-
-// Load order: window(t), its first two rung groups, window(t + 1) (the
-// consumers free the window slot before their rung phase, so the next
-// window is in flight while they work on the rungs), the rest of t's groups,
-// and so on.
-__device__ void producer(const FwdParams& P, const Smem& S) {
-    int wcount = 0, gcount = 0;
-    // Khat is written by the launch before this one
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    Tile x = decode(P, blockIdx.x);
-    int kt = 0;
-    if (blockIdx.x < P.ntiles && !load_window(P, S, x, wcount, kt)) goto fail;
-    for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
-        const Tile nx = next_tile(P, x);
-        const bool more = t + (int)gridDim.x < P.ntiles;
-        const int ng = (kt + RPG - 1) / RPG;
-        const int split = min(2, ng);
-        int nkt = 0;
-        for (int gi = 0; gi < ng; ++gi) {
-            if (gi == split && more && !load_window(P, S, nx, wcount, nkt)) goto fail;
-            if (!load_group(P, S, x, gi * RPG, kt, gcount)) goto fail;
-        }
-        if (split == ng && more && !load_window(P, S, nx, wcount, nkt)) goto fail;
-        x = nx;
-        kt = nkt;
-    }
-    return;
-fail:
-    *S.abort_flag = 1;
-    if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
-    // no copy of this CTA may land after it exits: wait (bounded) for every
-    // slot's last announced phase
-    if (wcount > 0) (void)mbar_wait(bar_full_w(S), (wcount - 1) & 1, nullptr);
-    for (int n = max(0, gcount - NGS); n < gcount; ++n)
-        (void)mbar_wait(bar_full_g(S, n & (NGS - 1)), (n / NGS) & 1, nullptr);
-}
-
 // ------------------------------------------------------------ consumers
-
-// Warp-uniform bounded wait (every lane polls, the warp leaves together).
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
-    const unsigned long long t0 = now_ns();
-    for (unsigned it = 0;; ++it) {
-        if (__all_sync(kFull, mbar_try_wait(bar, parity))) return true;
-        if (__any_sync(kFull, *abort_flag != 0)) return false;
-        if ((it & 15) == 15 && __any_sync(kFull, now_ns() - t0 > kWaitNs)) return false;
-        __nanosleep(32);
-    }
-}
-
-__device__ __forceinline__ TC lds_tc(uint32_t addr) {
-    TC v;
-    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=f"(v.t), "=r"(v.c) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ uint4 ldg_u4(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
-
-__device__ __forceinline__ uint32_t u4_get(const uint4& v, int w) {
-    return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
-}
 
 // One query pair (i, i + 1) of one key/value head: the B fragments of
 // Qhat^T, the O^T accumulators and softmax state of this thread's two
@@ -312,7 +113,6 @@ struct Unit {
     float2 l;
 };
 
-__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 
 // Per-thread constants of the fragment layouts (fixed for the whole kernel:
 // the warp always owns the query pairs at tile offsets u0 and u0 + 2).
@@ -328,17 +128,6 @@ struct Lane {
     uint32_t wk, wv;    // window tile 0: Khat and V row offsets
     uint32_t ob[2];     // output staging: stmatrix row address offsets (jj = 0, 1)
 };
-
-__device__ __forceinline__ uint32_t swz_row(int r, int hi) {
-    return (uint32_t)(r * ROWB) + (uint32_t)(((hi ^ r) & 7) << 4);
-}
-
-// Offset of the row that this lane gives to ldmatrix for rung position p of
-// unit u: M row (e, kind) of rung p is block row u + e + kind, stored 2p rows
-// into its box.
-__device__ __forceinline__ uint32_t rung_row(int p, int u, int e, int kind, int hi, bool v) {
-    return (uint32_t)(p * kRungBytes) + (v ? kRungRegion : 0u) + swz_row(u + e + kind + 2 * p, hi);
-}
 
 __device__ __forceinline__ Lane make_lane(int lane, int u0, int W, int win_rows) {
     Lane L;
@@ -395,7 +184,8 @@ __device__ __forceinline__ void fetch_q(const FwdParams& P, const Tile& x, int u
 }
 
 // Rotate the raw Q (RoPE rows of the tile in shared memory at `tab`, nq of
-// them) into B fragments; reset the accumulators.
+// them) into B fragments.  (The first window tile starts the O^T
+// accumulators.)
 __device__ __forceinline__ void start_unit(const FwdParams& P, uint32_t tab, int nq, int u, int lane,
                                            const uint4 raw[2], Unit& U) {
     const int g8 = lane >> 2, tig = lane & 3;
@@ -417,10 +207,6 @@ __device__ __forceinline__ void start_unit(const FwdParams& P, uint32_t tab, int
             U.qf[2 + (w >> 1)][w & 1] = u4_get(raw[1], w);
         }
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) U.o[j][e] = 0.f;
 }
 
 // Column max of this thread's two columns over the 8 threads holding them.
@@ -498,24 +284,28 @@ __device__ __forceinline__ float2 softmax_step2(const FwdParams& P, Unit& U, flo
 // Window M tile wt of the warp's query quad at tile offset u0 (positions
 // i0 + u0 .. + 3): region rows u0 + R, R = 16 wt .. 16 wt + 15, hold
 // positions i0 + u0 - W + R; unit k holds queries 2k, 2k + 1 of the quad.
+template <bool kFirst>
 __device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, int u0, int i0, int wt,
                                             const Lane& L, Unit* U) {
     const int lane = threadIdx.x & 31;
     uint32_t kro = L.wk, vro = L.wv;
-    if (wt > 0) {
+    if (!kFirst) {
         const int maxr = P.win_rows - 1;
         kro = swz_row(min(u0 + 16 * wt + (lane & 7) + (((lane >> 3) & 1) << 3), maxr), lane >> 4);
         vro = swz_row(min(u0 + 16 * wt + (lane & 7) + ((lane >> 4) << 3), maxr), (lane >> 3) & 1);
     }
     float c[2][4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = 0.f;
-#pragma unroll
     for (int s2 = 0; s2 < 4; ++s2) {
         uint32_t a0, a1, a2, a3;
         ldsm_x4(slot + (kro ^ (uint32_t)(s2 << 5)), a0, a1, a2, a3);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) mma16816(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+        for (int k = 0; k < 2; ++k) {
+            if (s2 == 0)
+                mma16816_z(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+            else
+                mma16816(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+        }
     }
     // window distances of each (row, query); near the sequence start, rows
     // below lo hold positions before it
@@ -532,7 +322,7 @@ __device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, i
 #pragma unroll
         for (int e = 0; e < 4; ++e) sv[e] = (mask >> (4 * k + e)) & 1u ? c[k][e] : -INFINITY;
         float p[4];
-        if (wt == 0)
+        if (kFirst)
             softmax_first(P, U[k], sv, p);
         else
             softmax_step4(P, U[k], sv, p);
@@ -545,7 +335,12 @@ __device__ __forceinline__ void window_tile(const FwdParams& P, uint32_t slot, i
         uint32_t a0, a1, a2, a3;
         ldsm_x4_t(vbase + (vro ^ (uint32_t)(j << 5)), a0, a1, a2, a3);
 #pragma unroll
-        for (int k = 0; k < 2; ++k) mma16816(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
+        for (int k = 0; k < 2; ++k) {
+            if (kFirst)
+                mma16816_z(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
+            else
+                mma16816(U[k].o[j], a0, a1, a2, a3, b[k][0], b[k][1]);
+        }
     }
 }
 
@@ -574,14 +369,15 @@ __device__ __forceinline__ void rung_tile(const FwdParams& P, const Smem& S, uin
     // S^T = Khat_rows . Qhat^T
     float c[2][4];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) c[k][0] = c[k][1] = c[k][2] = c[k][3] = 0.f;
-#pragma unroll
     for (int s2 = 0; s2 < 4; ++s2) {
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             uint32_t a0, a1, a2, a3;
             ldsm_x4(krow[k] ^ (uint32_t)(s2 << 5), a0, a1, a2, a3);
-            mma16816(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+            if (s2 == 0)
+                mma16816_z(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+            else
+                mma16816(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
         }
     }
     // this thread's rows: row b (c0, c1) and row a (c2, c3) of rung k0 + p
@@ -670,7 +466,8 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
 #pragma unroll
             for (int k = 0; k < 2; ++k)
                 start_unit(P, S.win + 2 * P.win_region, nq, u0 + 2 * k, lane, raw[k], U[k]);
-            for (int wt = 0; wt < P.nwt; ++wt) window_tile(P, S.win, u0, x.i0, wt, L, U);
+            window_tile<true>(P, S.win, u0, x.i0, 0, L, U);
+            for (int wt = 1; wt < P.nwt; ++wt) window_tile<false>(P, S.win, u0, x.i0, wt, L, U);
             kt = *S.kt;
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_empty_w(S));
@@ -719,39 +516,8 @@ fail:
 
 __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParams P) {
     extern __shared__ unsigned char smem_raw[];
-    // the dynamic allocation carries 1024 spare bytes to reach 1024 alignment
-    const uint32_t raw_base = smem_u32(smem_raw);
-    const uint32_t base = (raw_base + 1023u) & ~1023u;
-    unsigned char* hdr = smem_raw + (base - raw_base);
-    Smem S;
-    S.bars = base;
-    S.abort_flag = reinterpret_cast<int*>(hdr + kFlagOffset);
-    S.kt = reinterpret_cast<int*>(hdr + kKtOffset);
-    SRung* table = reinterpret_cast<SRung*>(hdr + kRungTableOffset);
-    S.r = table;
-    S.win = base + kHeaderBytes;
-    S.rung = S.win + P.win_slot_bytes;
-    S.obuf = S.rung + NGS * kGroupSlotBytes;
+    const Smem S = ring_setup(P.a, P.win_slot_bytes, smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    S.tc = base + kTcOffset;
-    if (threadIdx.x < P.a.nr) {
-        const Rung rg = P.a.r[threadIdx.x];
-        table[threadIdx.x] = SRung{rg.n, rg.t, rg.c};
-        reinterpret_cast<TC*>(hdr + kTcOffset)[threadIdx.x] = TC{rg.t, rg.c};
-    }
-    if (threadIdx.x == 0) {
-        // full: one arrival (the producer's expect_tx) plus the copied bytes;
-        // empty: one arrival per consumer warp
-        mbar_init(bar_full_w(S), 1);
-        mbar_init(bar_empty_w(S), NCW);
-        for (int i = 0; i < NGS; ++i) {
-            mbar_init(bar_full_g(S, i), 1);
-            mbar_init(bar_empty_g(S, i), NCW);
-        }
-        *S.abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
     if (warp == NCW) {
         if (lane == 0) producer(P, S);
     } else {
@@ -762,92 +528,55 @@ __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParam
 // -------------------------------------------------- RoPE on the keys
 
 // Khat[b][j][g][:] = R(j) K[b][j][g][:] in bf16, in the stored dimension
-// order of kdim_of.  One thread per (row, w): it writes stored chunk w
-// (dimensions 8 tig + 2 w + {0, 1}, tig = 0..3) and chunk 4 + w (their
-// partners + 32).
-__global__ void __launch_bounds__(256) rope_k_kernel(const __nv_bfloat16* __restrict__ k,
-                                                     const float2* __restrict__ rope,
-                                                     __nv_bfloat16* __restrict__ khat,
-                                                     long long rows, int T) {
+// order of kdim_of.  Four threads per row: thread a rotates the pairs
+// m = 8a .. 8a + 7 (dimensions 8a .. 8a + 7 and their partners + 32, two
+// 16-byte loads), which land in word a of every stored chunk; the four
+// threads exchange words through shared memory so that thread a writes whole
+// chunks a and 4 + a (two 16-byte stores).
+constexpr int kRopeThreads = 256;
+constexpr int kRopePitch = ROWB + 16;  // bytes per staged row: 4-byte stores of a phase hit distinct banks
+
+__global__ void __launch_bounds__(kRopeThreads) rope_k_kernel(const __nv_bfloat16* __restrict__ k,
+                                                              const float2* __restrict__ rope,
+                                                              __nv_bfloat16* __restrict__ khat,
+                                                              unsigned rows, unsigned T) {
     // the forward kernel may start its prologue now; it waits for this grid
     // to finish before it reads Khat
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long row = idx >> 2;
-    if (row >= rows) return;
-    const int w = (int)(idx & 3);
-    const int j = (int)((row / kHkv) % T);
-    const unsigned* kw = reinterpret_cast<const unsigned*>(k + row * kD);
-    const float4* cs = reinterpret_cast<const float4*>(rope + (size_t)j * kPairs);
-    uint32_t xo[4], yo[4];
+    __shared__ __align__(16) unsigned char stage[kRopeThreads / 4 * kRopePitch];
+    const unsigned lrow = threadIdx.x >> 2, a = threadIdx.x & 3;
+    const unsigned row = blockIdx.x * (kRopeThreads / 4) + lrow;
+    const bool live = row < rows;
+    unsigned char* srow = stage + lrow * kRopePitch;
+    if (live) {
+        const unsigned j = (row / kHkv) % T;
+        const __nv_bfloat16* kr = k + (size_t)row * kD;
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(kr + 8 * a));
+        const uint4 yv = __ldg(reinterpret_cast<const uint4*>(kr + 32 + 8 * a));
+        const float4* cs = reinterpret_cast<const float4*>(rope + (size_t)j * kPairs + 8 * a);
 #pragma unroll
-    for (int tig = 0; tig < 4; ++tig) {
-        // dimensions 8 tig + 2 w + {0, 1} (word 4 tig + w) and + 32 (word 16 + 4 tig + w)
-        const float4 t = __ldg(cs + 4 * tig + w);
-        const float2 x = unpack_bf16(__ldg(kw + 4 * tig + w));
-        const float2 y = unpack_bf16(__ldg(kw + 16 + 4 * tig + w));
-        xo[tig] = pack_bf16(x.x * t.x - y.x * t.y, x.y * t.z - y.y * t.w);
-        yo[tig] = pack_bf16(y.x * t.x + x.x * t.y, y.y * t.z + x.y * t.w);
+        for (int c = 0; c < 4; ++c) {
+            // pairs m = 8a + 2c + {0, 1}: stored at chunk c (x) and 4 + c (y), word a
+            const float4 t = __ldg(cs + c);
+            const float2 x = unpack_bf16(u4_get(xv, c));
+            const float2 y = unpack_bf16(u4_get(yv, c));
+            const uint32_t xo = pack_bf16(x.x * t.x - y.x * t.y, x.y * t.z - y.y * t.w);
+            const uint32_t yo = pack_bf16(y.x * t.x + x.x * t.y, y.y * t.z + x.y * t.w);
+            *reinterpret_cast<uint32_t*>(srow + 16 * c + 4 * a) = xo;
+            *reinterpret_cast<uint32_t*>(srow + 64 + 16 * c + 4 * a) = yo;
+        }
     }
-    *reinterpret_cast<uint4*>(khat + row * kD + 8 * w) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
-    *reinterpret_cast<uint4*>(khat + row * kD + 32 + 8 * w) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+    __syncwarp();
+    if (live) {
+        __nv_bfloat16* out = khat + (size_t)row * kD;
+        *reinterpret_cast<uint4*>(out + 8 * a) = *reinterpret_cast<const uint4*>(srow + 16 * a);
+        *reinterpret_cast<uint4*>(out + 32 + 8 * a) = *reinterpret_cast<const uint4*>(srow + 64 + 16 * a);
+    }
 }
 
 static_assert(kdim_of(1, 2, 1) == 8 * 2 + 2 * 1 + 1 && kdim_of(5, 3, 0) == 32 + 24 + 2, "dimension order");
 
 // ------------------------------------------------------------- host side
-
-struct DeviceInfo {
-    int sms = 0;
-    size_t configured_smem = 0;
-};
-
-DeviceInfo& device_info(int dev) {
-    static DeviceInfo info[64];
-    return info[dev & 63];
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            p = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }();
-    return fn;
-}
-
-// 4-D map over O [B][T][8][64] bf16 (innermost first: d, head, t, b), box of
-// 2 queries x 4 heads, 128-byte swizzle (the staging buffer's layout).
-bool encode_out(CUtensorMap* m, void* base, int B, int T) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHq, (cuuint64_t)T, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kHq * kD * 2, (cuuint64_t)T * kHq * kD * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)kD, (cuuint32_t)kG, 2u, 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 4-D map over a [B][T][Hkv][64] bf16 tensor (innermost first: d, g, t, b),
-// box of `rows` rows of one head, 128-byte swizzle, zero fill outside.
-bool encode_rows(CUtensorMap* m, const void* base, int B, int T, int rows) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHkv, (cuuint64_t)T, (cuuint64_t)B};
-    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kHkv * kD * 2,
-                                   (cuuint64_t)T * kHkv * kD * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)kD, 1u, (cuuint32_t)rows, 1u};
-    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 }  // namespace
 
@@ -863,11 +592,9 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    DeviceInfo& info = device_info(dev);
-    if (info.sms == 0) {
-        e = cudaDeviceGetAttribute(&info.sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-    }
+    const int sms = sm_count(dev, &e);
+    if (e != cudaSuccess) return e;
+    static size_t configured_smem[64];  // per device: dynamic shared memory already allowed
     FwdParams P;
     std::memset(&P, 0, sizeof(P));
     P.a = a;
@@ -886,10 +613,10 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
     const void* khat = k;
     if (rope) {
-        const long long rows = (long long)a.B * a.T * kHkv;
-        const long long threads = rows * 4;
-        rope_k_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(k), rope, static_cast<__nv_bfloat16*>(ws), rows, a.T);
+        const unsigned rows = (unsigned)a.B * (unsigned)a.T * kHkv;  // < 2^32: B T < 2^31
+        const unsigned per_block = kRopeThreads / 4;
+        rope_k_kernel<<<(rows + per_block - 1) / per_block, kRopeThreads, 0, s>>>(
+            static_cast<const __nv_bfloat16*>(k), rope, static_cast<__nv_bfloat16*>(ws), rows, (unsigned)a.T);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         count_launch();
         khat = ws;
@@ -905,18 +632,18 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     }
     const size_t smem = 1024 + kHeaderBytes + (size_t)P.win_slot_bytes + NGS * (size_t)kGroupSlotBytes +
                         NCW * (size_t)kObufBytes;
-    if (info.configured_smem < smem) {
+    if (configured_smem[dev & 63] < smem) {
         e = cudaFuncSetAttribute(fwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(fwd_mma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
-        info.configured_smem = smem;
+        configured_smem[dev & 63] = smem;
     }
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_mma_kernel, NTHREADS, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
-    long long grid = (long long)info.sms * per_sm;
+    long long grid = (long long)sms * per_sm;
     if (grid > P.ntiles) grid = P.ntiles;
     P.step_g = (int)(grid % kHkv);
     P.step_tq = (int)((grid / kHkv) % P.ntq);

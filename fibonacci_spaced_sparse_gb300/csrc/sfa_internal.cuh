@@ -55,6 +55,12 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
                            const float2* rope, void* o, float* lse, void* ws, unsigned* status,
                            cudaStream_t s);
 
+bool bwd_mma_supported(const LayerArgs& a);
+size_t bwd_mma_workspace(const LayerArgs& a, bool rope);
+cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, const void* v, const void* o,
+                           const void* dO, const float* lse, const float2* rope, void* dq, void* dk, void* dv,
+                           float* dalpha, float* dtheta, void* ws, unsigned* status, cudaStream_t s);
+
 size_t bwd_simple_workspace(const LayerArgs& a);
 cudaError_t launch_bwd_simple(const LayerArgs& a, sfa_dtype dt, const void* q, const void* k,
                               const void* v, const void* o, const void* dO, const float* lse,
