@@ -12,9 +12,10 @@
 //   dL/dt += scale ds (qhat . khat_b - qhat . khat_a) + p (dO . v_b - dO . v_a),
 // dL/dalpha = sum_k f_k dL/dt_k, dL/dtheta = dL/dalpha (alpha - 0.5)(1.5 - alpha).
 //
-// Three launches:
+// Three launches and a memset:
+//  0. the fp32 dKhat / dV accumulators are zeroed (cudaMemsetAsync).
 //  1. bwd_prep_kernel: Khat = RoPE(K) (bf16, natural dimension order) into the
-//     workspace and zeroes the fp32 dKhat / dV accumulators.
+//     workspace (not launched when the inputs come rotated).
 //  2. bwd_mma_kernel: persistent, the forward's tile map and load ring (one
 //     producer lane, seven consumer warps, a warp owns a quad of queries as
 //     two pairs).  Per M tile ("keys on M", as in the forward) it recomputes
@@ -49,6 +50,9 @@ constexpr int kPrepThreads = 256;
 constexpr int kFinishThreads = 256;
 
 struct BwdParams {
+    static constexpr int kQMaps = 3;  // the window slot carries the tile's Q, dO and O
+    CUtensorMap qmaps[kQMaps];
+    unsigned qtile_off;        // byte offset of the query tiles in the window slot
     CUtensorMap kmap_w;
     CUtensorMap vmap_w;
     CUtensorMap kmap_r[RPG];
@@ -62,6 +66,7 @@ struct BwdParams {
     const float2* rope;        // nullptr: inputs are used as given
     float* dk_acc;             // [B][T][Hkv][D] fp32, rotated frame
     float* dv_acc;
+    long long dv_off;          // dv_acc - dk_acc (floats)
     float* dt_part;            // [gridDim.x][SFA_MAX_RUNGS]
     unsigned* status;
     float sl2;                 // scale x log2(e)
@@ -133,16 +138,19 @@ __device__ __forceinline__ BLane make_blane(int lane, int u0, int W, int win_row
     return L;
 }
 
-__device__ __forceinline__ void red_v2(float* p, float a, float b) {
-    asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+// acc[0..1] += (a, b) when ok (predicated inside the instruction, no branch).
+__device__ __forceinline__ void red_v2(float* p, float a, float b, bool ok) {
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %3, 0;\n @q red.global.add.v2.f32 [%0], {%1, %2};\n}\n" ::"l"(p),
+        "f"(a), "f"(b), "r"((int)ok)
+        : "memory");
 }
 
-// Adds (a, b) to acc[row][dim], dim even, unless the row lies outside the
-// sequence or the pair is zero.
-__device__ __forceinline__ void red_row(float* acc, size_t row_base, int row, int T, int dim, float2 v,
-                                        bool ok) {
-    if (ok && row >= 0 && row < T && (v.x != 0.f || v.y != 0.f))
-        red_v2(acc + (row_base + (size_t)row * kHkv) * kD + dim, v.x, v.y);
+// Address of acc[b][row][g][2 tig] (row_base = b T Hkv + g), and whether the
+// row lies inside the sequence.
+__device__ __forceinline__ float* acc_row(float* acc, size_t row_base, int row, int T, int tig, bool& ok) {
+    ok = ok && row >= 0 && row < T;
+    return acc + (row_base + (size_t)(ok ? row : 0) * kHkv) * kD + 2 * tig;
 }
 
 __device__ __forceinline__ float2 f2add(float2 a, float2 b) { return __fadd2_rn(a, b); }
@@ -160,30 +168,33 @@ __device__ __forceinline__ void mma1688_z(float d[4], uint32_t a0, uint32_t a1, 
         : "r"(a0), "r"(a1), "r"(b0), "f"(0.0f));
 }
 
-// Loads the natural-order B-fragment words of one [.][8][64] bf16 row:
-// word (s, h) = dimensions 16 s + 8 h + 2 tig + {0, 1}.
-__device__ __forceinline__ void load_frag(const __nv_bfloat16* row, int tig, uint32_t w[4][2]) {
-    const unsigned* p = reinterpret_cast<const unsigned*>(row) + tig;
+// The natural-order B-fragment words of row r of a swizzled query tile
+// (addr = row start + 4 tig): word (s, h) = dimensions 16 s + 8 h + 2 tig +
+// {0, 1}, in 16-byte chunk 2 s + h stored at chunk (2 s + h) ^ (r & 7).
+__device__ __forceinline__ void load_frag_s(uint32_t addr, int r, uint32_t w[4][2]) {
 #pragma unroll
-    for (int s = 0; s < 4; ++s) {
-        w[s][0] = __ldg(p + 8 * s);
-        w[s][1] = __ldg(p + 8 * s + 4);
-    }
+    for (int s = 0; s < 4; ++s)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            asm volatile("ld.shared.b32 %0, [%1];"
+                         : "=r"(w[s][h])
+                         : "r"(addr + (uint32_t)((((2 * s + h) ^ (r & 7)) << 4))));
 }
 
 // Start of a tile for unit k (query pair at tile offset u): Qhat^T, dO^T and
 // their dK/dV forms, D and the log-sum-exp of this thread's C columns.
-__device__ __forceinline__ void start_bunit(const BwdParams& P, const Tile& x, uint32_t tab, int nq, int u,
+__device__ __forceinline__ void start_bunit(const BwdParams& P, const Tile& x, uint32_t slot, int nq, int u,
                                             int lane, BUnit& U) {
     const int g8 = lane >> 2, tig = lane & 3;
     const int T = P.a.T;
-    // B-fragment column: query u + g8/4, head g8 % 4
-    const int iq = min(x.i0 + u + (g8 >> 2), T - 1);
-    const size_t rq = (((size_t)x.b * T + iq) * kHq + x.g * kG + (g8 & 3)) * kD;
+    const uint32_t tab = slot + 2 * P.win_region;
+    // B-fragment column: query u + g8/4, head g8 % 4 = row 4 u + g8 of the
+    // query tiles (128-byte swizzle)
     uint32_t ow[4][2];
-    load_frag(P.q + rq, tig, U.qf);
-    load_frag(P.dO + rq, tig, U.df);
-    load_frag(P.o + rq, tig, ow);
+    const uint32_t qrow = slot + P.qtile_off + (uint32_t)((4 * u + g8) * ROWB) + 4u * tig;
+    load_frag_s(qrow, 4 * u + g8, U.qf);
+    load_frag_s(qrow + kQTileBytes, 4 * u + g8, U.df);
+    load_frag_s(qrow + 2 * kQTileBytes, 4 * u + g8, ow);
     // C columns: query u + tig/2, heads 2 (tig & 1) + {0, 1}
     const int ic = x.i0 + u + (tig >> 1);
     U.qok = ic < T;
@@ -296,18 +307,19 @@ __device__ __forceinline__ void bwd_window_tile(const BwdParams& P, uint32_t slo
     // columns), this thread's rows g8 and g8 + 8, dimensions 8 c + 2 tig + {0, 1}
     const int tig = lane & 3;
     const int r0 = i0 + u0 - P.a.W + 16 * wt + L.g8;
-    const bool use0 = 16 * wt + L.g8 <= P.a.W + 3, use1 = 16 * wt + L.g8 + 8 <= P.a.W + 3;
+    bool use0 = 16 * wt + L.g8 <= P.a.W + 3, use1 = 16 * wt + L.g8 + 8 <= P.a.W + 3;
     const size_t rb = (size_t)x.b * P.a.T * kHkv + x.g;
+    float* p0 = acc_row(P.dk_acc, rb, r0, P.a.T, tig, use0);
+    float* p1 = acc_row(P.dk_acc, rb, r0 + 8, P.a.T, tig, use1);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
         float dk[4], dv[4];
         mma16816_z(dk, ad[0][0], ad[0][1], ad[1][0], ad[1][1], U[0].qm[c], U[1].qm[c]);
         mma16816_z(dv, ap[0][0], ap[0][1], ap[1][0], ap[1][1], U[0].dm[c], U[1].dm[c]);
-        const int dim = 8 * c + 2 * tig;
-        red_row(P.dk_acc, rb, r0, P.a.T, dim, f2(dk[0], dk[1]), use0);
-        red_row(P.dk_acc, rb, r0 + 8, P.a.T, dim, f2(dk[2], dk[3]), use1);
-        red_row(P.dv_acc, rb, r0, P.a.T, dim, f2(dv[0], dv[1]), use0);
-        red_row(P.dv_acc, rb, r0 + 8, P.a.T, dim, f2(dv[2], dv[3]), use1);
+        red_v2(p0 + 8 * c, dk[0], dk[1], use0);
+        red_v2(p0 + P.dv_off + 8 * c, dv[0], dv[1], use0);
+        red_v2(p1 + 8 * c, dk[2], dk[3], use1);
+        red_v2(p1 + P.dv_off + 8 * c, dv[2], dv[3], use1);
     }
 }
 
@@ -402,12 +414,15 @@ __device__ __forceinline__ void bwd_rung_tile(const BwdParams& P, const Smem& S,
     // lanes 16..31 hold m = 1, 2 and 3, 4; the shared rows are summed across
     // the two halves of the warp before the reduction.
     const int base = x.i0 + u0 - S.r[min(k0 + p, nr - 1)].n - 1;
-    const bool pok = p < np;
     const size_t rb = (size_t)x.b * P.a.T * kHkv + x.g;
     const bool A = L.is_a;
+    bool okx = p < np, oky = p < np, okz = p < np && A;
+    float* px = acc_row(P.dk_acc, rb, base + (A ? 0 : 3), P.a.T, tig, okx);
+    float* py = acc_row(P.dk_acc, rb, base + (A ? 1 : 4), P.a.T, tig, oky);
+    float* pz = acc_row(P.dk_acc, rb, base + 2, P.a.T, tig, okz);
 #pragma unroll
     for (int tensor = 0; tensor < 2; ++tensor) {
-        float* acc = tensor == 0 ? P.dk_acc : P.dv_acc;
+        const long long off = tensor == 0 ? 0 : P.dv_off;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
             float m0[4], m1[4];
@@ -422,10 +437,12 @@ __device__ __forceinline__ void bwd_rung_tile(const BwdParams& P, const Smem& S,
             const float2 u1b = f2(m1[0], m1[1]), u1a = f2(m1[2], m1[3]);
             const float2 r1 = shfl2_xor(A ? u1a : u0b, 16);
             const float2 r2 = shfl2_xor(u0a, 16);
-            const int dim = 8 * c + 2 * tig;
-            red_row(acc, rb, base + (A ? 0 : 3), P.a.T, dim, A ? u0b : f2add(u1b, r1), pok);
-            red_row(acc, rb, base + (A ? 1 : 4), P.a.T, dim, A ? f2add(u0a, r1) : u1a, pok);
-            red_row(acc, rb, base + 2, P.a.T, dim, f2add(u1b, r2), pok && A);
+            const float2 vx = A ? u0b : f2add(u1b, r1);
+            const float2 vy = A ? f2add(u0a, r1) : u1a;
+            const float2 vz = f2add(u1b, r2);
+            red_v2(px + off + 8 * c, vx.x, vx.y, okx);
+            red_v2(py + off + 8 * c, vy.x, vy.y, oky);
+            red_v2(pz + off + 8 * c, vz.x, vz.y, okz);
         }
     }
 }
@@ -480,7 +497,7 @@ __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int la
             if (!warp_wait(bar_full_w(S), wcount & 1, S.abort_flag)) goto fail;
             const int nq = min(TQ, P.a.T - x.i0);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) start_bunit(P, x, S.win + 2 * P.win_region, nq, u0 + 2 * k, lane, U[k]);
+            for (int k = 0; k < 2; ++k) start_bunit(P, x, S.win, nq, u0 + 2 * k, lane, U[k]);
             bwd_window_tile<true>(P, S.win, x, u0, 0, L, U);
             for (int wt = 1; wt < P.nwt; ++wt) bwd_window_tile<false>(P, S.win, x, u0, wt, L, U);
             kt = *S.kt;
@@ -488,6 +505,7 @@ __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int la
             if (lane == 0) mbar_arrive(bar_empty_w(S));
             ++wcount;
         }
+        const Tile nx = next_tile(P, x);
         for (int k0 = 0; k0 < kt; k0 += RPG) {
             const int slot = gcount & (NGS - 1);
             if (!warp_wait(bar_full_g(S, slot), (gcount / NGS) & 1, S.abort_flag)) goto fail;
@@ -510,7 +528,7 @@ __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int la
                     tma_store_4d(&P.dqmap, obuf + (uint32_t)(k * 8 * ROWB), 0, x.g * kG, x.i0 + u0 + 2 * k, x.b);
             bulk_commit();
         }
-        x = next_tile(P, x);
+        x = nx;
     }
     if (lane == 0) bulk_wait_all();
     return;
@@ -545,28 +563,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_const
 
 // ------------------------------------------------------ prep and finish
 
-// Khat = RoPE(K) in the natural dimension order (skipped without a table) and
-// zero dKhat / dV accumulators.  Four threads per row (b, j, g): thread a
-// takes the rotation pairs 8a .. 8a + 7.
+// Khat = RoPE(K) in the natural dimension order.  Four threads per row
+// (b, j, g): thread a takes the rotation pairs 8a .. 8a + 7.
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloat16* __restrict__ k,
                                                                 const float2* __restrict__ rope,
-                                                                __nv_bfloat16* __restrict__ khat,
-                                                                float* __restrict__ dk_acc,
-                                                                float* __restrict__ dv_acc, unsigned rows,
+                                                                __nv_bfloat16* __restrict__ khat, unsigned rows,
                                                                 unsigned T) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const unsigned idx = blockIdx.x * kPrepThreads + threadIdx.x;
     const unsigned row = idx >> 2, a = idx & 3;
     if (row >= rows) return;
-    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4* dk4 = reinterpret_cast<float4*>(dk_acc + (size_t)row * kD + 16 * a);
-    float4* dv4 = reinterpret_cast<float4*>(dv_acc + (size_t)row * kD + 16 * a);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        dk4[i] = z;
-        dv4[i] = z;
-    }
-    if (!rope) return;
     const unsigned j = (row / kHkv) % T;
     const __nv_bfloat16* kr = k + (size_t)row * kD;
     const uint4 xv = __ldg(reinterpret_cast<const uint4*>(kr + 8 * a));
@@ -586,37 +592,37 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
     *reinterpret_cast<uint4*>(out + 32 + 8 * a) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
 }
 
-// dK = R(j)^T dKhat and dV, bf16, four threads per row (pairs 8a .. 8a + 7);
-// the last block reduces dL/dt over the CTA partials in a fixed order.
+// dK = R(j)^T dKhat and dV, bf16, four threads per row (pairs 8a .. 8a + 7).
+// Block 0 reduces dL/dt over the CTA partials instead: warp w takes the rungs
+// w, w + 8, ..., lanes sum strided partials in fp64 and a fixed-order
+// butterfly finishes each rung, so the result does not depend on timing.
 __global__ void __launch_bounds__(kFinishThreads) bwd_finish_mma_kernel(
     const LayerArgs a, const float* __restrict__ dk_acc, const float* __restrict__ dv_acc,
     const float2* __restrict__ rope, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
     const float* __restrict__ dt_part, int nparts, float* __restrict__ dalpha, float* __restrict__ dtheta,
-    unsigned rows, unsigned row_blocks) {
-    if (blockIdx.x == row_blocks) {
-        __shared__ double red[kFinishThreads];
-        double total = 0.0;
-        for (int r = 0; r < a.nr; ++r) {
+    unsigned rows) {
+    if (blockIdx.x == 0) {
+        __shared__ double per_rung[SFA_MAX_RUNGS];
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int r = warp; r < SFA_MAX_RUNGS; r += kFinishThreads / 32) {
             double s = 0.0;
-            for (int p = threadIdx.x; p < nparts; p += kFinishThreads)
-                s += (double)dt_part[(size_t)p * SFA_MAX_RUNGS + r];
-            red[threadIdx.x] = s;
-            __syncthreads();
-            for (int w = kFinishThreads / 2; w > 0; w >>= 1) {
-                if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-                __syncthreads();
-            }
-            if (threadIdx.x == 0) total += (double)a.r[r].f * red[0];
-            __syncthreads();
+            if (r < a.nr)
+                for (int p = lane; p < nparts; p += 32) s += (double)dt_part[(size_t)p * SFA_MAX_RUNGS + r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(kFull, s, o);
+            if (lane == 0) per_rung[r] = r < a.nr ? (double)a.r[r].f * s : 0.0;
         }
+        __syncthreads();
         if (threadIdx.x == 0) {
+            double total = 0.0;
+            for (int r = 0; r < a.nr; ++r) total += per_rung[r];
             const double al = (double)a.alpha;
             *dalpha = (float)total;
             *dtheta = (float)(total * (al - 0.5) * (1.5 - al));
         }
         return;
     }
-    const unsigned idx = blockIdx.x * kFinishThreads + threadIdx.x;
+    const unsigned idx = (blockIdx.x - 1) * kFinishThreads + threadIdx.x;
     const unsigned row = idx >> 2, q = idx & 3;
     if (row >= rows) return;
     const float4* xk = reinterpret_cast<const float4*>(dk_acc + (size_t)row * kD + 8 * q);
@@ -699,10 +705,14 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     if (e != cudaSuccess) return e;
     const BwdWorkspace w = carve(a, rope != nullptr, ws);
     const unsigned rows = (unsigned)a.B * (unsigned)a.T * kHkv;
-    {
+    // the two fp32 accumulators are contiguous
+    e = cudaMemsetAsync(w.dk_acc, 0, (size_t)(reinterpret_cast<char*>(w.dt_part) - reinterpret_cast<char*>(w.dk_acc)),
+                        s);
+    if (e != cudaSuccess) return e;
+    if (rope) {
         const unsigned blocks = (rows * 4 + kPrepThreads - 1) / kPrepThreads;
-        bwd_prep_kernel<<<blocks, kPrepThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k), rope, w.khat,
-                                                        w.dk_acc, w.dv_acc, rows, (unsigned)a.T);
+        bwd_prep_kernel<<<blocks, kPrepThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k), rope, w.khat, rows,
+                                                        (unsigned)a.T);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         count_launch();
     }
@@ -717,6 +727,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.rope = rope;
     P.dk_acc = w.dk_acc;
     P.dv_acc = w.dv_acc;
+    P.dv_off = w.dv_acc - w.dk_acc;
     P.dt_part = w.dt_part;
     P.status = status;
     P.sl2 = a.scale * kLog2e;
@@ -726,9 +737,11 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.win_rows = TQ + a.W;
     P.nwt = (a.W + 4 + 15) / 16;
     P.win_region = round1k((unsigned)P.win_rows * ROWB);
-    P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
+    P.qtile_off = 2 * P.win_region + round1k(TQ * TABB);
+    P.win_slot_bytes = P.qtile_off + BwdParams::kQMaps * kQTileBytes;
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) || !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows) ||
-        !encode_out(&P.dqmap, dq, a.B, a.T))
+        !encode_out(&P.dqmap, dq, a.B, a.T) || !encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) ||
+        !encode_heads(&P.qmaps[1], dO, a.B, a.T, TQ) || !encode_heads(&P.qmaps[2], o, a.B, a.T, TQ))
         return cudaErrorInvalidValue;
     for (int p = 0; p < RPG; ++p) {
         const int r = RUNG_ROWS + 2 * p;
@@ -762,7 +775,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = rope ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, bwd_mma_kernel, P);
     if (e != cudaSuccess) return e;
     count_launch();
@@ -770,7 +783,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
         const unsigned row_blocks = (rows * 4 + kFinishThreads - 1) / kFinishThreads;
         bwd_finish_mma_kernel<<<row_blocks + 1, kFinishThreads, 0, s>>>(
             a, w.dk_acc, w.dv_acc, rope, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-            w.dt_part, (int)grid, dalpha, dtheta, rows, row_blocks);
+            w.dt_part, (int)grid, dalpha, dtheta, rows);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         count_launch();
     }

@@ -62,6 +62,9 @@ constexpr float kMinMax = -1e30f;      // floor of the running max (no entry yet
 constexpr unsigned kObufBytes = 2 * 8 * ROWB;               // per consumer warp: O of 2 query pairs
 
 struct FwdParams {
+    static constexpr int kQMaps = 0;  // the window slot carries no query tiles
+    CUtensorMap qmaps[1];      // unused
+    unsigned qtile_off;        // unused
     CUtensorMap kmap_w;        // Khat, box of win_rows rows
     CUtensorMap vmap_w;        // V, box of win_rows rows
     CUtensorMap kmap_r[RPG];   // Khat, box of RUNG_ROWS + 2p rows, rung position p

@@ -17,7 +17,8 @@
 // A parameter struct PP used with these templates provides: kmap_w, vmap_w
 // (window boxes of win_rows rows), kmap_r[RPG], vmap_r[RPG] (rung boxes),
 // a (LayerArgs), rope, status, ntq, ntiles, step_g, step_tq, step_b, win_rows,
-// win_region.
+// win_region, and kQMaps (static) tile maps qmaps[] of per-query [B][T][8][64]
+// tensors that the window slot also carries, from byte qtile_off on.
 #pragma once
 
 #include <cuda.h>
@@ -49,6 +50,7 @@ constexpr unsigned kRungRegion = round1k(RUNG_BOX * ROWB);  // one tensor of one
 constexpr unsigned kRungBytes = 2 * kRungRegion;            // Khat region, then V region
 constexpr unsigned kGroupSlotBytes = RPG * kRungBytes;
 constexpr unsigned kHeaderBytes = 1024;                     // barriers, flag, rung table
+constexpr unsigned kQTileBytes = TQ * kG * ROWB;            // one [TQ][4 heads][64] bf16 query tile
 
 // -------------------------------------------------------------- tile map
 
@@ -140,11 +142,14 @@ __device__ __forceinline__ bool load_window(const PP& P, const Smem& S, const Ti
     kt = active_rungs(S, P.a.nr, x.i0);
     *S.kt = kt;  // published by the arrive below
     const uint32_t full = bar_full_w(S);
-    mbar_arrive_expect_tx(full, 2u * P.win_rows * ROWB + tab_bytes);
+    mbar_arrive_expect_tx(full, 2u * P.win_rows * ROWB + tab_bytes + PP::kQMaps * kQTileBytes);
     tma_load_4d(S.win, &P.kmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
     tma_load_4d(S.win + P.win_region, &P.vmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
     // RoPE rows of the tile's query positions (read by the consumers' Q rotation)
     if (P.rope) bulk_g2s(S.win + 2 * P.win_region, P.rope + (size_t)x.i0 * kPairs, tab_bytes, full);
+    // per-query tensors of the tile (rows (query, head) of the key/value head's 4 query heads)
+    for (int m = 0; m < PP::kQMaps; ++m)
+        tma_load_4d(S.win + P.qtile_off + m * kQTileBytes, &P.qmaps[m], 0, x.g * kG, x.i0, x.b, full);
     ++wcount;
     return true;
 }
@@ -323,6 +328,20 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // 4-D map over O [B][T][8][64] bf16 (innermost first: d, head, t, b), box of
 // 2 queries x 4 heads, 128-byte swizzle (the staging buffer's layout).
+// 4-D map over a [B][T][8][64] bf16 tensor (innermost first: d, head, t, b),
+// box of `queries` queries x 4 heads, 128-byte swizzle, zero fill outside.
+inline bool encode_heads(CUtensorMap* m, const void* base, int B, int T, int queries) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHq, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 2, (cuuint64_t)kHq * kD * 2, (cuuint64_t)T * kHq * kD * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)kD, (cuuint32_t)kG, (cuuint32_t)queries, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 inline bool encode_out(CUtensorMap* m, void* base, int B, int T) {
     auto fn = encode_fn();
     if (!fn) return false;
