@@ -50,9 +50,8 @@ constexpr int kPrepThreads = 256;
 constexpr int kFinishThreads = 256;
 
 struct BwdParams {
-    static constexpr int kQMaps = 3;  // the window slot carries the tile's Q, dO and O
+    static constexpr int kQMaps = 3;  // the query slot carries the tile's Q, dO and O
     CUtensorMap qmaps[kQMaps];
-    unsigned qtile_off;        // byte offset of the query tiles in the window slot
     CUtensorMap kmap_w;
     CUtensorMap vmap_w;
     CUtensorMap kmap_r[RPG];
@@ -100,7 +99,7 @@ struct BLane {
     bool useful;        // this thread's rung rows belong to its column query
     bool is_a;          // lanes 0..15: query e = 0 of each pair
     unsigned wmask;
-    uint32_t kn[2];     // rung tile of unit k: non-transposed row offsets (Khat; + kRungRegion: V)
+    uint32_t kn[2];     // rung tile of unit k: non-transposed row offsets (Khat; + kVOff: V)
     uint32_t kt[2];     // rung tile of unit k: transposed row offsets (Khat)
     uint32_t wk, wt;    // window tile 0: non-transposed / transposed row offsets
     uint32_t ob[2];
@@ -183,15 +182,16 @@ __device__ __forceinline__ void load_frag_s(uint32_t addr, int r, uint32_t w[4][
 
 // Start of a tile for unit k (query pair at tile offset u): Qhat^T, dO^T and
 // their dK/dV forms, D and the log-sum-exp of this thread's C columns.
-__device__ __forceinline__ void start_bunit(const BwdParams& P, const Tile& x, uint32_t slot, int nq, int u,
+__device__ __forceinline__ void start_bunit(const BwdParams& P, const Smem& S, const Tile& x, int nq, int u,
                                             int lane, BUnit& U) {
+    const uint32_t slot = S.win;
     const int g8 = lane >> 2, tig = lane & 3;
     const int T = P.a.T;
     const uint32_t tab = slot + 2 * P.win_region;
     // B-fragment column: query u + g8/4, head g8 % 4 = row 4 u + g8 of the
     // query tiles (128-byte swizzle)
     uint32_t ow[4][2];
-    const uint32_t qrow = slot + P.qtile_off + (uint32_t)((4 * u + g8) * ROWB) + 4u * tig;
+    const uint32_t qrow = S.qslot + (uint32_t)((4 * u + g8) * ROWB) + 4u * tig;
     load_frag_s(qrow, 4 * u + g8, U.qf);
     load_frag_s(qrow + kQTileBytes, 4 * u + g8, U.df);
     load_frag_s(qrow + 2 * kQTileBytes, 4 * u + g8, ow);
@@ -353,7 +353,7 @@ __device__ __forceinline__ void bwd_rung_tile(const BwdParams& P, const Smem& S,
         for (int k = 0; k < 2; ++k) {
             uint32_t a0, a1, a2, a3, v0, v1, v2, v3;
             ldsm_x4(kn[k] ^ (uint32_t)(s2 << 5), a0, a1, a2, a3);
-            ldsm_x4((kn[k] + kRungRegion) ^ (uint32_t)(s2 << 5), v0, v1, v2, v3);
+            ldsm_x4((kn[k] + kVOff) ^ (uint32_t)(s2 << 5), v0, v1, v2, v3);
             if (s2 == 0) {
                 mma16816_z(cs[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
                 mma16816_z(cp[k], v0, v1, v2, v3, U[k].df[s2][0], U[k].df[s2][1]);
@@ -482,7 +482,7 @@ __device__ __forceinline__ void store_dq(const BwdParams& P, const Tile& x, int 
 }
 
 __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int lane, float* dt_w) {
-    int wcount = 0, gcount = 0;
+    int wcount = 0, gcount = 0, qcount = 0;
     const int u0 = 4 * warp;
     const BLane L = make_blane(lane, u0, P.a.W, P.win_rows);
     const uint32_t obuf = S.obuf + (uint32_t)(warp * kObufBytes);
@@ -494,15 +494,19 @@ __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int la
         BUnit U[2];
         int kt;
         {
+            if (!warp_wait(bar_full_q(S), qcount & 1, S.abort_flag)) goto fail;
             if (!warp_wait(bar_full_w(S), wcount & 1, S.abort_flag)) goto fail;
             const int nq = min(TQ, P.a.T - x.i0);
 #pragma unroll
-            for (int k = 0; k < 2; ++k) start_bunit(P, x, S.win, nq, u0 + 2 * k, lane, U[k]);
+            for (int k = 0; k < 2; ++k) start_bunit(P, S, x, nq, u0 + 2 * k, lane, U[k]);
+            __syncwarp();
+            mbar_arrive_if(bar_empty_q(S), lane == 0);
+            ++qcount;
             bwd_window_tile<true>(P, S.win, x, u0, 0, L, U);
             for (int wt = 1; wt < P.nwt; ++wt) bwd_window_tile<false>(P, S.win, x, u0, wt, L, U);
             kt = *S.kt;
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty_w(S));
+            mbar_arrive_if(bar_empty_w(S), lane == 0);
             ++wcount;
         }
         const Tile nx = next_tile(P, x);
@@ -512,7 +516,7 @@ __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int la
             bwd_rung_tile(P, S, S.rung + (uint32_t)slot * kGroupSlotBytes, x, k0, min(RPG, kt - k0), nr, u0, L,
                           U, dt_w);
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty_g(S, slot));
+            mbar_arrive_if(bar_empty_g(S, slot), lane == 0);
             ++gcount;
         }
         if (lane == 0) bulk_wait_read();
@@ -542,7 +546,7 @@ fail:
 
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_constant__ BwdParams P) {
     extern __shared__ unsigned char smem_raw[];
-    const Smem S = ring_setup(P.a, P.win_slot_bytes, smem_raw);
+    const Smem S = ring_setup(P.a, BwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // per consumer warp dL/dt sums, after the output staging buffers
     float* dt_all = reinterpret_cast<float*>(smem_raw + (S.obuf + NCW * kObufBytes - smem_u32(smem_raw)));
@@ -737,8 +741,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.win_rows = TQ + a.W;
     P.nwt = (a.W + 4 + 15) / 16;
     P.win_region = round1k((unsigned)P.win_rows * ROWB);
-    P.qtile_off = 2 * P.win_region + round1k(TQ * TABB);
-    P.win_slot_bytes = P.qtile_off + BwdParams::kQMaps * kQTileBytes;
+    P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) || !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows) ||
         !encode_out(&P.dqmap, dq, a.B, a.T) || !encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) ||
         !encode_heads(&P.qmaps[1], dO, a.B, a.T, TQ) || !encode_heads(&P.qmaps[2], o, a.B, a.T, TQ))
@@ -748,8 +751,8 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
         if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, r) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, r))
             return cudaErrorInvalidValue;
     }
-    const size_t smem = 1024 + kHeaderBytes + (size_t)P.win_slot_bytes + NGS * (size_t)kGroupSlotBytes +
-                        NCW * (size_t)kObufBytes + kDtBytes;
+    const size_t smem = 1024 + kHeaderBytes + BwdParams::kQMaps * (size_t)kQTileBytes + (size_t)P.win_slot_bytes +
+                        NGS * (size_t)kGroupSlotBytes + NCW * (size_t)kObufBytes + kDtBytes;
     static size_t configured_smem[64];
     if (configured_smem[dev & 63] < smem) {
         e = cudaFuncSetAttribute(bwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

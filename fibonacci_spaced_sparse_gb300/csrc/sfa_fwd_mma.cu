@@ -59,17 +59,16 @@ using namespace ring;
 
 constexpr float kLazy = 8.0f;          // raise the running max past this margin
 constexpr float kMinMax = -1e30f;      // floor of the running max (no entry yet)
-constexpr unsigned kObufBytes = 2 * 8 * ROWB;               // per consumer warp: O of 2 query pairs
+constexpr unsigned kObufBytes = 8 * ROWB;  // per consumer warp: O of one query pair (2 queries x 4 heads)
 
 struct FwdParams {
-    static constexpr int kQMaps = 0;  // the window slot carries no query tiles
-    CUtensorMap qmaps[1];      // unused
-    unsigned qtile_off;        // unused
+    static constexpr int kQMaps = 1;  // the query slot carries the tile's Q
+    CUtensorMap qmaps[kQMaps];        // Q [B][T][8][64], box of TQ queries x 4 heads
+    CUtensorMap omap;                 // O [B][T][8][64], box of 2 queries x 4 heads, 128-byte swizzle
     CUtensorMap kmap_w;        // Khat, box of win_rows rows
     CUtensorMap vmap_w;        // V, box of win_rows rows
     CUtensorMap kmap_r[RPG];   // Khat, box of RUNG_ROWS + 2p rows, rung position p
     CUtensorMap vmap_r[RPG];   // V, same boxes
-    CUtensorMap omap;          // O [B][T][8][64], box of 2 queries x 4 heads, 128-byte swizzle
     LayerArgs a;
     const __nv_bfloat16* q;
     const float2* rope;        // nullptr: Q and K are used as given
@@ -168,46 +167,36 @@ __device__ __forceinline__ Lane make_lane(int lane, int u0, int W, int win_rows)
     return L;
 }
 
-// Raw Q of this thread's B-fragment column (query i0 + u + g8/4, head
-// g*4 + g8%4): with RoPE, dimensions 8 tig .. 8 tig + 7 (raw[0]) and their
-// partners + 32 (raw[1]); without, the dimensions of the stored order
-// directly (word w of raw[h'] = position 16 (2h' + w/2) + 8 (w&1) + 2 tig).
-__device__ __forceinline__ void fetch_q(const FwdParams& P, const Tile& x, int u, int lane, uint4 raw[2]) {
+// Q of this thread's B-fragment column (query u + g8/4, head g8 % 4 = row
+// r = 4u + g8 of the Q tile in the query slot, 128-byte swizzle: 16-byte
+// chunk c at c ^ (r & 7), and r & 7 = g8) rotated by the RoPE rows of the
+// tile (nq of them) into B fragments.  With RoPE the thread reads dimensions
+// 8 tig .. 8 tig + 7 (chunk tig) and their partners + 32 (chunk 4 + tig);
+// without, the positions of the stored order directly (word w of fragment
+// half h' = chunk 4 h' + w, word tig).  The first window tile starts the O^T
+// accumulators.
+__device__ __forceinline__ void start_unit(const FwdParams& P, const Smem& S, int nq, int u, int lane, Unit& U) {
     const int g8 = lane >> 2, tig = lane & 3;
-    const int iq = min(x.i0 + u + (g8 >> 2), P.a.T - 1);  // rows past the end are not stored
-    const __nv_bfloat16* qp = P.q + (((size_t)x.b * P.a.T + iq) * kHq + x.g * kG + (g8 & 3)) * kD;
+    const uint32_t slot = S.win;
+    const uint32_t qrow = S.qslot + (uint32_t)((4 * u + g8) * ROWB);
     if (P.rope) {
-        raw[0] = ldg_u4(qp + 8 * tig);
-        raw[1] = ldg_u4(qp + 32 + 8 * tig);
-    } else {
-        const unsigned* w = reinterpret_cast<const unsigned*>(qp) + tig;
-        raw[0] = make_uint4(__ldg(w), __ldg(w + 4), __ldg(w + 8), __ldg(w + 12));
-        raw[1] = make_uint4(__ldg(w + 16), __ldg(w + 20), __ldg(w + 24), __ldg(w + 28));
-    }
-}
-
-// Rotate the raw Q (RoPE rows of the tile in shared memory at `tab`, nq of
-// them) into B fragments.  (The first window tile starts the O^T
-// accumulators.)
-__device__ __forceinline__ void start_unit(const FwdParams& P, uint32_t tab, int nq, int u, int lane,
-                                           const uint4 raw[2], Unit& U) {
-    const int g8 = lane >> 2, tig = lane & 3;
-    if (P.rope) {
-        const uint32_t trow = tab + (uint32_t)(min(u + (g8 >> 2), nq - 1) * TABB + tig * 64);
+        const uint4 x4 = lds_u4(qrow + (uint32_t)((tig ^ g8) << 4));
+        const uint4 y4 = lds_u4(qrow + (uint32_t)(((4 + tig) ^ g8) << 4));
+        const uint32_t trow = slot + 2 * P.win_region + (uint32_t)(min(u + (g8 >> 2), nq - 1) * TABB + tig * 64);
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             // pairs m = 8 tig + 2 w + {0, 1}: (cos, sin) of both
             const float4 cs = lds_f4(trow + (uint32_t)(w * 16));
-            const float2 xv = unpack_bf16(u4_get(raw[0], w));
-            const float2 yv = unpack_bf16(u4_get(raw[1], w));
+            const float2 xv = unpack_bf16(u4_get(x4, w));
+            const float2 yv = unpack_bf16(u4_get(y4, w));
             U.qf[w >> 1][w & 1] = pack_bf16(xv.x * cs.x - yv.x * cs.y, xv.y * cs.z - yv.y * cs.w);
             U.qf[2 + (w >> 1)][w & 1] = pack_bf16(yv.x * cs.x + xv.x * cs.y, yv.y * cs.z + xv.y * cs.w);
         }
     } else {
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            U.qf[w >> 1][w & 1] = u4_get(raw[0], w);
-            U.qf[2 + (w >> 1)][w & 1] = u4_get(raw[1], w);
+            U.qf[w >> 1][w & 1] = lds_u32(qrow + (uint32_t)(((w ^ g8) << 4) + 4 * tig));
+            U.qf[2 + (w >> 1)][w & 1] = lds_u32(qrow + (uint32_t)((((4 + w) ^ g8) << 4) + 4 * tig));
         }
     }
 }
@@ -415,18 +404,18 @@ __device__ __forceinline__ void rung_tile(const FwdParams& P, const Smem& S, uin
     }
 }
 
-// Normalise O^T and stage it, transposed, in this warp's output buffer (rows
-// (query, head) of the pair, 128-byte swizzle) for the TMA store; the
-// log-sum-exp goes straight out.
-__device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, int u, int k, uint32_t obuf,
-                                           const Lane& L, int lane, Unit& U) {
+// Normalise O^T of the pair at tile offset u and stage it, transposed, in
+// this warp's output buffer (rows (query, head), 128-byte swizzle) for a TMA
+// store; the buffer holds one pair, so the previous store must have read it.
+// The log-sum-exp goes straight out.
+__device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, int u, uint32_t obuf, const Lane& L,
+                                           int lane, Unit& U) {
     const int g8 = lane >> 2, tig = lane & 3;
     float2 l = U.l;
 #pragma unroll
     for (int w = 4; w <= 16; w <<= 1)
         l = __fadd2_rn(l, f2(__shfl_xor_sync(kFull, l.x, w), __shfl_xor_sync(kFull, l.y, w)));
     const float2 inv = f2(1.f / l.x, 1.f / l.y);
-    const uint32_t buf = obuf + (uint32_t)(k * 8 * ROWB);
     uint32_t r[4][2];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -435,9 +424,17 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
         r[j][0] = pack_bf16(a.x, a.y);
         r[j][1] = pack_bf16(b.x, b.y);
     }
+    if (lane == 0) bulk_wait_read();
+    __syncwarp();
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj)
-        stsm_x4_t(buf + L.ob[jj], r[2 * jj][0], r[2 * jj][1], r[2 * jj + 1][0], r[2 * jj + 1][1]);
+        stsm_x4_t(obuf + L.ob[jj], r[2 * jj][0], r[2 * jj][1], r[2 * jj + 1][0], r[2 * jj + 1][1]);
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0 && x.i0 + u < P.a.T) {
+        tma_store_4d(&P.omap, obuf, 0, x.g * kG, x.i0 + u, x.b);
+        bulk_commit();
+    }
     if (P.lse && g8 == 0) {
         const int iq2 = x.i0 + u + (tig >> 1);
         if (iq2 < P.a.T) {
@@ -449,38 +446,30 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
 }
 
 __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) {
-    int wcount = 0, gcount = 0;
+    int wcount = 0, gcount = 0, qcount = 0;
     const int u0 = 4 * warp;  // query pairs at tile offsets u0 and u0 + 2
     const Lane L = make_lane(lane, u0, P.a.W, P.win_rows);
     const uint32_t obuf = S.obuf + (uint32_t)(warp * kObufBytes);
     const int nr = max(P.a.nr, 1);
-    uint4 raw[2][2];
     Tile x = decode(P, blockIdx.x);
-    if (blockIdx.x < P.ntiles) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) fetch_q(P, x, u0 + 2 * k, lane, raw[k]);
-    }
     for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
         Unit U[2];
         int kt;
         {
+            if (!warp_wait(bar_full_q(S), qcount & 1, S.abort_flag)) goto fail;
             if (!warp_wait(bar_full_w(S), wcount & 1, S.abort_flag)) goto fail;
             const int nq = min(TQ, P.a.T - x.i0);
 #pragma unroll
-            for (int k = 0; k < 2; ++k)
-                start_unit(P, S.win + 2 * P.win_region, nq, u0 + 2 * k, lane, raw[k], U[k]);
+            for (int k = 0; k < 2; ++k) start_unit(P, S, nq, u0 + 2 * k, lane, U[k]);
+            __syncwarp();
+            mbar_arrive_if(bar_empty_q(S), lane == 0);
+            ++qcount;
             window_tile<true>(P, S.win, u0, x.i0, 0, L, U);
             for (int wt = 1; wt < P.nwt; ++wt) window_tile<false>(P, S.win, u0, x.i0, wt, L, U);
             kt = *S.kt;
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty_w(S));
+            mbar_arrive_if(bar_empty_w(S), lane == 0);
             ++wcount;
-        }
-        // the next tile's Q is in flight while this tile's rungs are computed
-        const Tile nx = next_tile(P, x);
-        if (t + (int)gridDim.x < P.ntiles) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) fetch_q(P, nx, u0 + 2 * k, lane, raw[k]);
         }
         for (int k0 = 0; k0 < kt; k0 += RPG) {
             const int slot = gcount & (NGS - 1);
@@ -488,24 +477,12 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
             rung_tile(P, S, S.rung + (uint32_t)slot * kGroupSlotBytes, k0, min(RPG, kt - k0), nr, u0,
                       x.i0 + u0, L, U);
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty_g(S, slot));
+            mbar_arrive_if(bar_empty_g(S, slot), lane == 0);
             ++gcount;
         }
-        // the previous tile's stores must have read this warp's buffer
-        if (lane == 0) bulk_wait_read();
-        __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 2; ++k) store_unit(P, x, u0 + 2 * k, k, obuf, L, lane, U[k]);
-        fence_proxy_async();
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-                if (x.i0 + u0 + 2 * k < P.a.T)
-                    tma_store_4d(&P.omap, obuf + (uint32_t)(k * 8 * ROWB), 0, x.g * kG, x.i0 + u0 + 2 * k, x.b);
-            bulk_commit();
-        }
-        x = nx;
+        for (int k = 0; k < 2; ++k) store_unit(P, x, u0 + 2 * k, obuf, L, lane, U[k]);
+        x = next_tile(P, x);
     }
     if (lane == 0) bulk_wait_all();
     return;
@@ -519,7 +496,7 @@ fail:
 
 __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParams P) {
     extern __shared__ unsigned char smem_raw[];
-    const Smem S = ring_setup(P.a, P.win_slot_bytes, smem_raw);
+    const Smem S = ring_setup(P.a, FwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp == NCW) {
         if (lane == 0) producer(P, S);
@@ -627,14 +604,15 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) ||
         !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows))
         return cudaErrorInvalidValue;
-    if (!encode_out(&P.omap, o, a.B, a.T)) return cudaErrorInvalidValue;
+    if (!encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) || !encode_out(&P.omap, o, a.B, a.T))
+        return cudaErrorInvalidValue;
     for (int p = 0; p < RPG; ++p) {
         const int rows = RUNG_ROWS + 2 * p;
         if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, rows) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, rows))
             return cudaErrorInvalidValue;
     }
-    const size_t smem = 1024 + kHeaderBytes + (size_t)P.win_slot_bytes + NGS * (size_t)kGroupSlotBytes +
-                        NCW * (size_t)kObufBytes;
+    const size_t smem = 1024 + kHeaderBytes + FwdParams::kQMaps * (size_t)kQTileBytes + (size_t)P.win_slot_bytes +
+                        NGS * (size_t)kGroupSlotBytes + NCW * (size_t)kObufBytes;
     if (configured_smem[dev & 63] < smem) {
         e = cudaFuncSetAttribute(fwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;

@@ -9,16 +9,16 @@
 // offsets are shared by every query ("Attended set", section 2 of
 // "Depth-Staggered Fibonacci Spacing for Sparse Attention", arXiv 2606.28560).
 // One producer lane moves these blocks of Khat and V with tiled TMA boxes into
-// an mbarrier ring: one window slot (with the RoPE rows of the tile's queries)
-// and NGS group slots of RPG rungs each; the consumer warps release slots with
-// one arrival each.  Every wait is bounded: a wait that gives up sets the
+// an mbarrier ring: one query slot (the tile's query rows), one window slot
+// (with the RoPE rows of the tile's queries) and NGS group slots of RPG rungs
+// each; the consumer warps release slots with one arrival each.  Every wait is bounded: a wait that gives up sets the
 // CTA's abort flag and SFA_DEVSTAT_WAIT_TIMEOUT in the status word.
 //
 // A parameter struct PP used with these templates provides: kmap_w, vmap_w
 // (window boxes of win_rows rows), kmap_r[RPG], vmap_r[RPG] (rung boxes),
 // a (LayerArgs), rope, status, ntq, ntiles, step_g, step_tq, step_b, win_rows,
-// win_region, and kQMaps (static) tile maps qmaps[] of per-query [B][T][8][64]
-// tensors that the window slot also carries, from byte qtile_off on.
+// win_region, and kQMaps (static, >= 1) tile maps qmaps[] of per-query
+// [B][T][8][64] tensors that the query slot carries.
 #pragma once
 
 #include <cuda.h>
@@ -46,9 +46,19 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kNoRung = 1 << 30;       // ceiling of a rung no query of the tile uses
 
 constexpr unsigned round1k(unsigned x) { return (x + 1023u) & ~1023u; }
-constexpr unsigned kRungRegion = round1k(RUNG_BOX * ROWB);  // one tensor of one rung
-constexpr unsigned kRungBytes = 2 * kRungRegion;            // Khat region, then V region
-constexpr unsigned kGroupSlotBytes = RPG * kRungBytes;
+// A group slot holds the Khat regions of rung positions 0..RPG-1, then their V
+// regions.  Position p's box has RUNG_ROWS + 2p rows; each region starts on a
+// 1024-byte boundary (the period of the 128-byte swizzle).
+constexpr unsigned rung_region_bytes(int p) { return round1k((RUNG_ROWS + 2 * p) * ROWB); }
+constexpr unsigned rung_region_off(int p) { return p == 0 ? 0u : rung_region_off(p - 1) + rung_region_bytes(p - 1); }
+constexpr unsigned kVOff = rung_region_off(RPG);            // V region of p = Khat region of p + kVOff
+// The same offsets in closed form (TQ = 28: 4, 4, 5, 5 KB regions), for
+// run-time positions.
+__host__ __device__ constexpr unsigned rung_off(int p) { return (unsigned)p * 4096u + (p >= 3 ? 1024u : 0u); }
+static_assert(rung_off(0) == rung_region_off(0) && rung_off(1) == rung_region_off(1) &&
+                  rung_off(2) == rung_region_off(2) && rung_off(3) == rung_region_off(3),
+              "rung region offsets");
+constexpr unsigned kGroupSlotBytes = 2 * kVOff;
 constexpr unsigned kHeaderBytes = 1024;                     // barriers, flag, rung table
 constexpr unsigned kQTileBytes = TQ * kG * ROWB;            // one [TQ][4 heads][64] bf16 query tile
 
@@ -100,7 +110,8 @@ struct TC {
 };
 
 struct Smem {
-    uint32_t bars;      // full_w, empty_w, full_g[NGS], empty_g[NGS]
+    uint32_t bars;      // full_w, empty_w, full_g[NGS], empty_g[NGS], full_q, empty_q
+    uint32_t qslot;     // the query slot
     uint32_t win;       // the window slot
     uint32_t rung;      // NGS group slots
     uint32_t obuf;      // NCW output staging buffers
@@ -114,12 +125,15 @@ __device__ __forceinline__ uint32_t bar_full_w(const Smem& s) { return s.bars; }
 __device__ __forceinline__ uint32_t bar_empty_w(const Smem& s) { return s.bars + 8; }
 __device__ __forceinline__ uint32_t bar_full_g(const Smem& s, int i) { return s.bars + 16 + 8 * i; }
 __device__ __forceinline__ uint32_t bar_empty_g(const Smem& s, int i) { return s.bars + 16 + 8 * (NGS + i); }
-constexpr int kBarBytes = 16 + 16 * NGS;
+__device__ __forceinline__ uint32_t bar_full_q(const Smem& s) { return s.bars + 16 + 16 * NGS; }
+__device__ __forceinline__ uint32_t bar_empty_q(const Smem& s) { return s.bars + 24 + 16 * NGS; }
+constexpr int kBarBytes = 32 + 16 * NGS;
 constexpr int kFlagOffset = kBarBytes;
 constexpr int kKtOffset = kFlagOffset + 4;
 constexpr int kRungTableOffset = 256;
 constexpr int kTcOffset = kRungTableOffset + SFA_MAX_RUNGS * 12;  // {t, ceil} per rung, 8 bytes
 static_assert(kKtOffset + 4 <= kRungTableOffset, "header overflow");
+static_assert(rung_region_off(1) == 4096 && kVOff == 18432, "rung region layout");
 static_assert(kTcOffset + SFA_MAX_RUNGS * 8 <= (int)kHeaderBytes, "header overflow");
 
 // Rungs are sorted by ceil(d): those usable by some query of the tile form a prefix.
@@ -142,15 +156,27 @@ __device__ __forceinline__ bool load_window(const PP& P, const Smem& S, const Ti
     kt = active_rungs(S, P.a.nr, x.i0);
     *S.kt = kt;  // published by the arrive below
     const uint32_t full = bar_full_w(S);
-    mbar_arrive_expect_tx(full, 2u * P.win_rows * ROWB + tab_bytes + PP::kQMaps * kQTileBytes);
+    mbar_arrive_expect_tx(full, 2u * P.win_rows * ROWB + tab_bytes);
     tma_load_4d(S.win, &P.kmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
     tma_load_4d(S.win + P.win_region, &P.vmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
     // RoPE rows of the tile's query positions (read by the consumers' Q rotation)
     if (P.rope) bulk_g2s(S.win + 2 * P.win_region, P.rope + (size_t)x.i0 * kPairs, tab_bytes, full);
-    // per-query tensors of the tile (rows (query, head) of the key/value head's 4 query heads)
-    for (int m = 0; m < PP::kQMaps; ++m)
-        tma_load_4d(S.win + P.qtile_off + m * kQTileBytes, &P.qmaps[m], 0, x.g * kG, x.i0, x.b, full);
     ++wcount;
+    return true;
+}
+
+// The per-query tensors of tile x (rows (query, head) of the key/value head's
+// 4 query heads, PP::kQMaps of them) into the query slot.  The consumers free
+// that slot as soon as they have read it at the start of a tile, so the next
+// tile's query rows load while the current tile is computed.
+template <class PP>
+__device__ __forceinline__ bool load_q(const PP& P, const Smem& S, const Tile& x, int& qcount) {
+    if (!mbar_wait(bar_empty_q(S), (qcount & 1) ^ 1, S.abort_flag)) return false;
+    const uint32_t full = bar_full_q(S);
+    mbar_arrive_expect_tx(full, PP::kQMaps * kQTileBytes);
+    for (int m = 0; m < PP::kQMaps; ++m)
+        tma_load_4d(S.qslot + m * kQTileBytes, &P.qmaps[m], 0, x.g * kG, x.i0, x.b, full);
+    ++qcount;
     return true;
 }
 
@@ -168,9 +194,9 @@ __device__ __forceinline__ bool load_group(const PP& P, const Smem& S, const Til
     mbar_arrive_expect_tx(full, bytes);
     for (int p = 0; p < np; ++p) {
         const int row0 = x.i0 - S.r[k0 + p].n - 1 - 2 * p;
-        const uint32_t dst = base + p * kRungBytes;
+        const uint32_t dst = base + rung_off(p);
         tma_load_4d(dst, &P.kmap_r[p], 0, x.g, row0, x.b, full);
-        tma_load_4d(dst + kRungRegion, &P.vmap_r[p], 0, x.g, row0, x.b, full);
+        tma_load_4d(dst + kVOff, &P.vmap_r[p], 0, x.g, row0, x.b, full);
     }
     ++gcount;
     return true;
@@ -182,11 +208,12 @@ __device__ __forceinline__ bool load_group(const PP& P, const Smem& S, const Til
 // and so on.
 template <class PP>
 __device__ void producer(const PP& P, const Smem& S) {
-    int wcount = 0, gcount = 0;
+    int wcount = 0, gcount = 0, qcount = 0;
     // Khat is written by the launch before this one
     asm volatile("griddepcontrol.wait;" ::: "memory");
     Tile x = decode(P, blockIdx.x);
     int kt = 0;
+    if (blockIdx.x < P.ntiles && !load_q(P, S, x, qcount)) goto fail;
     if (blockIdx.x < P.ntiles && !load_window(P, S, x, wcount, kt)) goto fail;
     for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
         const Tile nx = next_tile(P, x);
@@ -195,10 +222,11 @@ __device__ void producer(const PP& P, const Smem& S) {
         const int split = min(2, ng);
         int nkt = 0;
         for (int gi = 0; gi < ng; ++gi) {
-            if (gi == split && more && !load_window(P, S, nx, wcount, nkt)) goto fail;
+            if (gi == split && more && (!load_q(P, S, nx, qcount) || !load_window(P, S, nx, wcount, nkt)))
+                goto fail;
             if (!load_group(P, S, x, gi * RPG, kt, gcount)) goto fail;
         }
-        if (split == ng && more && !load_window(P, S, nx, wcount, nkt)) goto fail;
+        if (split == ng && more && (!load_q(P, S, nx, qcount) || !load_window(P, S, nx, wcount, nkt))) goto fail;
         x = nx;
         kt = nkt;
     }
@@ -208,6 +236,7 @@ fail:
     if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
     // no copy of this CTA may land after it exits: wait (bounded) for every
     // slot's last announced phase
+    if (qcount > 0) (void)mbar_wait(bar_full_q(S), (qcount - 1) & 1, nullptr);
     if (wcount > 0) (void)mbar_wait(bar_full_w(S), (wcount - 1) & 1, nullptr);
     for (int n = max(0, gcount - NGS); n < gcount; ++n)
         (void)mbar_wait(bar_full_g(S, n & (NGS - 1)), (n / NGS) & 1, nullptr);
@@ -237,6 +266,18 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ uint4 ldg_u4(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
 __device__ __forceinline__ uint32_t u4_get(const uint4& v, int w) {
@@ -253,7 +294,7 @@ __device__ __forceinline__ uint32_t swz_row(int r, int hi) {
 // unit u: M row (e, kind) of rung p is block row u + e + kind, stored 2p rows
 // into its box.
 __device__ __forceinline__ uint32_t rung_row(int p, int u, int e, int kind, int hi, bool v) {
-    return (uint32_t)(p * kRungBytes) + (v ? kRungRegion : 0u) + swz_row(u + e + kind + 2 * p, hi);
+    return rung_off(p) + (v ? kVOff : 0u) + swz_row(u + e + kind + 2 * p, hi);
 }
 
 
@@ -262,7 +303,8 @@ __device__ __forceinline__ uint32_t rung_row(int p, int u, int e, int kind, int 
 // the header and initialises the barriers: full barriers take one arrival
 // (the producer's expect_tx) plus the copied bytes, empty barriers one
 // arrival per consumer warp.  Ends with a CTA barrier.
-__device__ __forceinline__ Smem ring_setup(const LayerArgs& a, unsigned win_slot_bytes, unsigned char* smem_raw) {
+__device__ __forceinline__ Smem ring_setup(const LayerArgs& a, unsigned qslot_bytes, unsigned win_slot_bytes,
+                                           unsigned char* smem_raw) {
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     unsigned char* hdr = smem_raw + (base - raw_base);
@@ -272,7 +314,8 @@ __device__ __forceinline__ Smem ring_setup(const LayerArgs& a, unsigned win_slot
     S.kt = reinterpret_cast<int*>(hdr + kKtOffset);
     SRung* table = reinterpret_cast<SRung*>(hdr + kRungTableOffset);
     S.r = table;
-    S.win = base + kHeaderBytes;
+    S.qslot = base + kHeaderBytes;
+    S.win = S.qslot + qslot_bytes;
     S.rung = S.win + win_slot_bytes;
     S.obuf = S.rung + NGS * kGroupSlotBytes;
     S.tc = base + kTcOffset;
@@ -288,6 +331,8 @@ __device__ __forceinline__ Smem ring_setup(const LayerArgs& a, unsigned win_slot
             mbar_init(bar_full_g(S, i), 1);
             mbar_init(bar_empty_g(S, i), NCW);
         }
+        mbar_init(bar_full_q(S), 1);
+        mbar_init(bar_empty_q(S), NCW);
         *S.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
