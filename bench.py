@@ -3,8 +3,10 @@
 One step = the forward of all 16 layers of B=32 sequences of T=1024 tokens
 (W=12, linear stagger alpha_l = 0.5 + l/15, Fibonacci base, bf16, 8 query / 2
 key-value heads, d=64), each layer its own seeded inputs already resident in
-HBM.  The 16 layers' inputs (1.34 GB) are larger than L2, so no flush is
-needed between steps.  ``value`` counts query tokens of every layer call.
+HBM, through one sfa_forward_layers call (one attention launch per layer,
+each also rotating the next layer's keys, plus one RoPE launch for layer 0).
+The 16 layers' inputs (1.34 GB) are larger than L2, so no flush is needed
+between steps.  ``value`` counts query tokens of every layer.
 
 Also reported: ``e2e`` (the same step through the C ABI with pinned host
 buffers, host->device inputs and device->host outputs inside the timed
@@ -35,13 +37,14 @@ METRIC = "sparse-attn fwd query-tokens/s (T=1024,W=12,bf16); HBM GB/s as % of GB
 UNIT = "query-tokens/s"
 IDEAL_BYTES_PER_TOKEN = 2 * (8 * 64 + 2 * 64 + 2 * 64 + 8 * 64)  # bf16 Q, K, V read + O write
 FALLBACK_HBM_GBS = 6800.0
+E2E_MAX_STEPS = 20
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="model-shape",
                     choices=["model-shape", "extrapolation", "pow2", "train-step", "long-forward"])
@@ -75,7 +78,7 @@ def measured_peak():
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -89,7 +92,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -161,28 +164,32 @@ def recorded_traffic(workload_name):
 
 def cpu_baseline(wl, budget_s=12.0):
     """The fp64 oracle as it stands on the host cores: whole layers of the
-    workload (all B sequences), layer after layer, until the budget is spent."""
+    workload (all B sequences), cycling through its first four layers until
+    about budget_s seconds of oracle time are spent."""
     import torch
     from fibonacci_spaced_sparse_gb300 import inputs
     from oracle import oracle
     oracle.build()
     alphas, _ = wl.alphas()
     cores = oracle.default_threads()
-    tokens, spent, layers = 0, 0.0, 0
-    for l in range(wl.layers):
-        x = inputs.qkv(wl.B, wl.T, dtype=torch.bfloat16, layer=l)
-        f = {k: v.to(torch.float64).numpy() for k, v in x.items()}
+    data = {}
+    tokens, spent, calls = 0, 0.0, 0
+    nl = min(4, wl.layers)
+    while spent < budget_s and calls < 8 * wl.layers:
+        l = calls % nl
+        if l not in data:
+            x = inputs.qkv(wl.B, wl.T, dtype=torch.bfloat16, layer=l)
+            data[l] = {k: v.to(torch.float64).numpy() for k, v in x.items()}
+        f = data[l]
         t0 = time.perf_counter()
         oracle.forward(f["q"], f["k"], f["v"], W=wl.window(l), rungs=wl.rungs(), alpha=alphas[l],
                        nthreads=cores)
         spent += time.perf_counter() - t0
         tokens += wl.B * wl.T
-        layers += 1
-        if spent >= budget_s:
-            break
+        calls += 1
     return {"value": tokens / spent, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{layers} of {wl.layers} layers, all {wl.B}x{wl.T} query tokens each, "
-                      f"{spent:.1f} s"}
+            "sample": f"{calls} whole-layer forwards ({wl.B}x{wl.T} query tokens each, "
+                      f"layers 0..{nl - 1} in turn), {spent:.1f} s of oracle time"}
 
 
 # --------------------------------------------------------------- our arm --
@@ -211,17 +218,26 @@ def run_ours(args, rank, world, local):
                                                    rungs=wl.rungs()) for l, a in enumerate(alphas))
         ws = torch.empty(need, dtype=torch.uint8, device=dev)
 
+    windows = [wl.window(l) for l in range(L)]
+    qs, ks, vs = [d["q"] for d in dv], [d["k"] for d in dv], [d["v"] for d in dv]
+
     def step(events=None):
-        for l in range(L):
-            if events is not None:
-                events[l][0].record(stream)
-            api.sfa_forward(dv[l]["q"], dv[l]["k"], dv[l]["v"], alpha=alphas[l], W=wl.window(l),
-                            rungs=wl.rungs(), out=outs[l], lse=lses[l])
-            if events is not None:
-                events[l][1].record(stream)
-            if wl.backward:
+        # the forward of every layer in one call; with a backward, layer by
+        # layer (the backward needs each layer's O and LSE)
+        if events is not None:
+            events[0].record(stream)
+        api.sfa_forward_layers(qs, ks, vs, alphas=alphas, W=windows, rungs=wl.rungs(), outs=outs,
+                               lses=lses)
+        if events is not None:
+            events[1].record(stream)
+        if wl.backward:
+            for l in range(L):
+                if events is not None:
+                    events[2 + 2 * l].record(stream)
                 api.sfa_backward(dv[l]["q"], dv[l]["k"], dv[l]["v"], outs[l], dv[l]["dO"], lses[l],
                                  alpha=alphas[l], W=wl.window(l), rungs=wl.rungs(), workspace=ws)
+                if events is not None:
+                    events[3 + 2 * l].record(stream)
 
     use_dist = world > 1
     if use_dist:
@@ -239,8 +255,8 @@ def run_ours(args, rank, world, local):
     barrier()
 
     # device-timed region: K steps, per-launch events on the launching stream
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
-          for _ in range(args.steps)]
+    nev = 2 + (2 * L if wl.backward else 0)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n0 = api.launch_count()
     with ClockSampler(local) as clk:
@@ -252,7 +268,9 @@ def run_ours(args, rank, world, local):
         barrier()
     launches = api.launch_count() - n0
     elapsed_ms = start.elapsed_time(stop)
-    fwd_ms = [e[0].elapsed_time(e[1]) for st in ev for e in st]
+    # per-layer average of the forward (the multi-layer call's time / L)
+    fwd_ms = [st[0].elapsed_time(st[1]) / L for st in ev]
+    bwd_ms = [st[2 + 2 * l].elapsed_time(st[3 + 2 * l]) for st in ev for l in range(L)] if wl.backward else []
     if use_dist:
         import torch.distributed as dist
         t = torch.tensor([elapsed_ms], device=dev)
@@ -277,6 +295,15 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.no_cpu and world == 1:
         cpu = cpu_baseline(wl)
 
+    if wl.backward:
+        bwd_avg = statistics.mean(bwd_ms) / 1e3
+        # backward ideal bytes: read Q, K, V, O, dO and write dQ, dK, dV once (bf16)
+        bwd_ideal = 2 * (8 * 64 + 2 * 64 + 2 * 64 + 8 * 64 + 8 * 64 + 8 * 64 + 2 * 64 + 2 * 64) * wl.B * wl.T
+        backward = {"avg_launch_us": bwd_avg * 1e6, "ideal_bytes_per_call": bwd_ideal,
+                    "achieved": bwd_ideal / bwd_avg / 1e9, "peak": peak, "unit": "GB/s",
+                    "frac": bwd_ideal / bwd_avg / 1e9 / peak}
+    else:
+        backward = None
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -292,9 +319,15 @@ def run_ours(args, rank, world, local):
                        "parallelism": f"replicas x{world}"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "forward", "ideal_bytes_per_launch": ideal,
-                         "avg_launch_us": avg_launch_s * 1e6, "peak_kind": peak_kind},
+                         "kernel": "forward attention (fwd_mma_kernel)",
+                         "ideal_bytes_per_launch": ideal,
+                         "avg_launch_us": avg_launch_s * 1e6,
+                         "avg_launch_note": "per-layer average of the timed multi-layer calls "
+                                            "(CUDA events on the launching stream), including "
+                                            "layer 0's RoPE launch and launch gaps",
+                         "peak_kind": peak_kind},
             "cpu_baseline": cpu,
+            "backward": backward,
             "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk.summary(),
@@ -353,12 +386,13 @@ def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
         stream.wait_stream(up)
         stream.wait_stream(down)
 
-    for _ in range(max(3, args.warmup)):
+    for _ in range(max(3, min(args.warmup, 5))):
         step()
     torch.cuda.synchronize(dev)
+    steps = min(args.steps, E2E_MAX_STEPS)  # each step moves 1.3 GB over the host link
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for _ in range(args.steps):
+    for _ in range(steps):
         step()
     stop.record(stream)
     torch.cuda.synchronize(dev)
@@ -368,9 +402,9 @@ def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    tokens = wl.B * wl.T * L * args.steps * world
+    tokens = wl.B * wl.T * L * steps * world
     return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h, "steps": steps}
 
 
 # --------------------------------------------------------- reference arm --

@@ -59,6 +59,9 @@ _SIGS = {
     "sfa_forward_workspace_size": ([_PP], ctypes.c_size_t),
     "sfa_forward": ([_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_size_t, _VP, _VP],
                     ctypes.c_int),
+    "sfa_forward_layers_workspace_size": ([_PP, ctypes.c_int, _IP], ctypes.c_size_t),
+    "sfa_forward_layers": ([_PP, ctypes.c_int, _FP, _IP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                            ctypes.c_size_t, _VP, _VP], ctypes.c_int),
     "sfa_forward_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "sfa_forward_noalloc": ([_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "sfa_backward_workspace_size": ([_PP], ctypes.c_size_t),

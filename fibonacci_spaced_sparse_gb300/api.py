@@ -181,6 +181,47 @@ def sfa_forward(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE, rope_the
     return o, (lse if need_lse else None)
 
 
+def _ptrs(ts) -> ctypes.Array:
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() if t is not None else 0 for t in ts])
+
+
+def sfa_forward_layers(qs, ks, vs, *, alphas, W, rungs=FIBONACCI_BASE, rope_theta: float = 1e4,
+                       scale: float = 0.0, need_lse: bool = True, outs=None, lses=None,
+                       status=None, workspace=None, stream=None):
+    """The forwards of L layers in one call (sfa_forward_layers in
+    include/sfa.h): qs, ks, vs are lists of per-layer tensors, alphas the L
+    per-layer scalars, W one window or a list of L windows."""
+    L = len(qs)
+    if not (len(ks) == len(vs) == len(alphas) == L) or L == 0:
+        raise ValueError("qs, ks, vs and alphas must have one entry per layer")
+    for q, k, v in zip(qs, ks, vs):
+        _check_qkv(q, k, v)
+        if q.shape != qs[0].shape or q.dtype != qs[0].dtype or q.device != qs[0].device:
+            raise ValueError("all layers must share shape, dtype and device")
+    B, T = qs[0].shape[0], qs[0].shape[1]
+    dev = qs[0].device
+    outs = outs if outs is not None else [torch.empty_like(q) for q in qs]
+    if need_lse and lses is None:
+        lses = [torch.empty((B, T, 8), dtype=torch.float32, device=dev) for _ in range(L)]
+    windows = [int(W)] * L if isinstance(W, int) else [int(w) for w in W]
+    p = Params(B, T, W=windows[0], alpha=alphas[0], rungs=rungs, rope_theta=rope_theta,
+               scale=scale, dtype=qs[0].dtype)
+    win = (ctypes.c_int * L)(*windows)
+    al = (ctypes.c_float * L)(*[float(a) for a in alphas])
+    lib = _lib.load()
+    need = int(lib.sfa_forward_layers_workspace_size(p.ref(), L, win))
+    if workspace is None or workspace.numel() < need:
+        workspace = _workspace(dev, need) if need else None
+    tab = rope_table(T, dev, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
+    lse_arr = _ptrs(lses) if need_lse else None
+    st = lib.sfa_forward_layers(p.ref(), L, al, win, _ptrs(qs), _ptrs(ks), _ptrs(vs), _vp(tab),
+                                _ptrs(outs), lse_arr, _vp(workspace),
+                                ctypes.c_size_t(workspace.numel() if workspace is not None else 0),
+                                _vp(status), _stream(dev, stream))
+    _lib.check(st, "sfa_forward_layers")
+    return outs, (lses if need_lse else None)
+
+
 def sfa_forward_noalloc(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
                         rope_theta: float = 1e4, scale: float = 0.0, out, lse=None, rope=None,
                         status=None, stream=None):

@@ -124,6 +124,33 @@ sfa_status launched(cudaError_t e) {
     return SFA_OK;
 }
 
+// Checks of one forward call's tensors (shared by the single- and
+// multi-layer entry points).
+sfa_status check_forward_ptrs(const sfa_params* p, const void* Q, const void* K, const void* V,
+                                     const float* rope_table, const void* O, const float* lse) {
+    if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
+        return SFA_ERR_INVALID_ARG;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
+    if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
+    return SFA_OK;
+}
+
+size_t align256_host(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// The multi-layer forward runs the attention launches back to back and lets
+// each one rotate the next layer's keys (two rotated-key buffers in turn)
+// when every layer takes the bf16 tensor-core path with RoPE.
+bool layers_batched(const sfa_params* p, int L, const int* windows) {
+    for (int l = 0; l < L; ++l) {
+        sfa_params pl = *p;
+        if (windows) pl.W = windows[l];
+        LayerArgs a;
+        fill_args(&pl, &a);
+        if (!use_mma(&pl, a)) return false;
+    }
+    return p->rope_theta > 0.f;
+}
+
 }  // namespace
 
 extern "C" {
@@ -230,10 +257,7 @@ SFA_API sfa_status sfa_forward(const sfa_params* p, const void* Q, const void* K
     sfa_status st = validate(p);
     if (st != SFA_OK) return st;
     if (p->B == 0 || p->T == 0) return SFA_OK;
-    if (!Q || !K || !V || !O || !aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O))
-        return SFA_ERR_INVALID_ARG;
-    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return SFA_ERR_INVALID_ARG;
-    if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
+    if ((st = check_forward_ptrs(p, Q, K, V, rope_table, O, lse)) != SFA_OK) return st;
     LayerArgs a;
     fill_args(p, &a);
     if (use_mma(p, a)) {
@@ -246,6 +270,75 @@ SFA_API sfa_status sfa_forward(const sfa_params* p, const void* Q, const void* K
     }
     return launched(sfa::launch_fwd_simple(a, p->dtype, Q, K, V, rope_ptr(p, rope_table), O, lse,
                                            stream));
+}
+
+SFA_API size_t sfa_forward_layers_workspace_size(const sfa_params* p, int L, const int* windows) {
+    if (validate(p) != SFA_OK || L <= 0) return 0;
+    size_t need = 0;
+    for (int l = 0; l < L; ++l) {
+        sfa_params pl = *p;
+        if (windows) pl.W = windows[l];
+        if (pl.W < 0) return 0;
+        const size_t n = sfa_forward_workspace_size(&pl);
+        if (n > need) need = n;
+    }
+    return layers_batched(p, L, windows) ? 2 * align256_host(need) : need;
+}
+
+SFA_API sfa_status sfa_forward_layers(const sfa_params* p, int L, const float* alphas, const int* windows,
+                                      const void* const* Q, const void* const* K, const void* const* V,
+                                      const float* rope_table, void* const* O, float* const* lse,
+                                      void* workspace, size_t workspace_bytes, unsigned int* status,
+                                      cudaStream_t stream) {
+    sfa_status st = validate(p);
+    if (st != SFA_OK) return st;
+    if (L <= 0 || !alphas || !Q || !K || !V || !O) return SFA_ERR_INVALID_ARG;
+    for (int l = 0; l < L; ++l) {
+        sfa_params pl = *p;
+        pl.alpha = alphas[l];
+        if (windows) pl.W = windows[l];
+        if ((st = validate(&pl)) != SFA_OK) return st;
+        if (p->B > 0 && p->T > 0 &&
+            (st = check_forward_ptrs(&pl, Q[l], K[l], V[l], rope_table, O[l], lse ? lse[l] : nullptr)) != SFA_OK)
+            return st;
+    }
+    if (p->B == 0 || p->T == 0) return SFA_OK;
+    const size_t need = sfa_forward_layers_workspace_size(p, L, windows);
+    if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need))
+        return SFA_ERR_INVALID_ARG;
+    if (!layers_batched(p, L, windows)) {
+        for (int l = 0; l < L; ++l) {
+            sfa_params pl = *p;
+            pl.alpha = alphas[l];
+            if (windows) pl.W = windows[l];
+            st = sfa_forward(&pl, Q[l], K[l], V[l], rope_table, O[l], lse ? lse[l] : nullptr, workspace,
+                             workspace_bytes, status, stream);
+            if (st != SFA_OK) return st;
+        }
+        return SFA_OK;
+    }
+    char* ws[2] = {static_cast<char*>(workspace), static_cast<char*>(workspace) + need / 2};
+    const float2* rope = reinterpret_cast<const float2*>(rope_table);
+    LayerArgs a;
+    {
+        sfa_params pl = *p;
+        pl.alpha = alphas[0];
+        if (windows) pl.W = windows[0];
+        fill_args(&pl, &a);
+        if ((st = launched(sfa::launch_rope_k(a, K[0], rope, ws[0], stream))) != SFA_OK) return st;
+    }
+    for (int l = 0; l < L; ++l) {
+        sfa_params pl = *p;
+        pl.alpha = alphas[l];
+        if (windows) pl.W = windows[l];
+        fill_args(&pl, &a);
+        const bool more = l + 1 < L;
+        st = launched(sfa::launch_fwd_attention(a, Q[l], ws[l & 1], V[l], rope, O[l], lse ? lse[l] : nullptr,
+                                                more ? K[l + 1] : nullptr, more ? ws[(l + 1) & 1] : nullptr,
+                                                status, true, stream));
+        if (st != SFA_OK) return st;
+    }
+    return SFA_OK;
 }
 
 SFA_API size_t sfa_backward_workspace_size(const sfa_params* p) {

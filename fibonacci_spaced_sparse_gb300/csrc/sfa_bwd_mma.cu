@@ -43,6 +43,8 @@ namespace {
 using namespace mma;
 using namespace ring;
 
+constexpr int NCW = 7;                         // consumer warps (a quad of queries each)
+constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr unsigned kObufBytes = 2 * 8 * ROWB;  // per consumer warp: dQ of 2 query pairs
 constexpr unsigned kDtBytes = NCW * SFA_MAX_RUNGS * 4;
 constexpr int kMaxGrid = 1024;                 // CTAs of the persistent kernel (dL/dt partials)
@@ -51,6 +53,7 @@ constexpr int kFinishThreads = 256;
 
 struct BwdParams {
     static constexpr int kQMaps = 3;  // the query slot carries the tile's Q, dO and O
+    static constexpr bool kWinRope = true;
     CUtensorMap qmaps[kQMaps];
     CUtensorMap kmap_w;
     CUtensorMap vmap_w;
@@ -546,7 +549,7 @@ fail:
 
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_constant__ BwdParams P) {
     extern __shared__ unsigned char smem_raw[];
-    const Smem S = ring_setup(P.a, BwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
+    const Smem S = ring_setup(P.a, NCW, BwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // per consumer warp dL/dt sums, after the output staging buffers
     float* dt_all = reinterpret_cast<float*>(smem_raw + (S.obuf + NCW * kObufBytes - smem_u32(smem_raw)));

@@ -59,10 +59,13 @@ using namespace ring;
 
 constexpr float kLazy = 8.0f;          // raise the running max past this margin
 constexpr float kMinMax = -1e30f;      // floor of the running max (no entry yet)
+constexpr int NCW = 7;                     // consumer warps (two query pairs each)
+constexpr int NTHREADS = (NCW + 1) * 32;   // + the producer warp
 constexpr unsigned kObufBytes = 8 * ROWB;  // per consumer warp: O of one query pair (2 queries x 4 heads)
 
 struct FwdParams {
     static constexpr int kQMaps = 1;  // the query slot carries the tile's Q
+    static constexpr bool kWinRope = true;  // the window slot carries the tile's RoPE rows
     CUtensorMap qmaps[kQMaps];        // Q [B][T][8][64], box of TQ queries x 4 heads
     CUtensorMap omap;                 // O [B][T][8][64], box of 2 queries x 4 heads, 128-byte swizzle
     CUtensorMap kmap_w;        // Khat, box of win_rows rows
@@ -75,6 +78,8 @@ struct FwdParams {
     __nv_bfloat16* o;
     float* lse;
     unsigned* status;
+    const __nv_bfloat16* k_next;  // keys of the next layer (multi-layer forward) or nullptr
+    __nv_bfloat16* khat_next;     // where their rotated copy goes
     float sl2;                 // softmax scale x log2(e)
     float inv_sl2;
     int ntq;                   // query tiles per sequence
@@ -494,13 +499,61 @@ fail:
     }
 }
 
+// Khat_next = RoPE(K_next) for the positions (b, j) of this CTA's share
+// (both key/value heads of a position, whole rows, stored in the kdim_of
+// order), done by the consumer warps while the first tile's loads are in
+// flight: the next layer of a multi-layer forward then needs no RoPE launch.
+// The buffer written here was read by the launch before this one.
+__device__ void rope_next(const FwdParams& P, int worker, int nworkers) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int npos = P.a.B * P.a.T;
+    const int per = (npos + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int p0 = (int)blockIdx.x * per, p1 = min(npos, p0 + per);
+    for (int pos = p0 + worker; pos < p1; pos += nworkers) {
+        const int j = pos % P.a.T;
+        const float4* cs = reinterpret_cast<const float4*>(P.rope + (size_t)j * kPairs);  // pairs 2w, 2w + 1
+#pragma unroll 1
+        for (int g = 0; g < kHkv; ++g) {
+            const size_t row = (size_t)pos * kHkv + g;
+            const uint4* kr = reinterpret_cast<const uint4*>(P.k_next + row * kD);
+            uint4* out = reinterpret_cast<uint4*>(P.khat_next + row * kD);
+            // rotated words xr[w] (dimensions 2w, 2w + 1) and yr[w] (+ 32) of
+            // 8-dimension chunk i = w / 4; stored chunk c, word tig holds
+            // dimensions 8 tig + 2c + {0, 1} (+ 32 for c >= 4)
+            uint32_t xr[16], yr[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint4 kx = __ldg(kr + i), ky = __ldg(kr + 4 + i);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int w = 4 * i + q;
+                    const float4 c = __ldg(cs + w);
+                    const float2 x = unpack_bf16(u4_get(kx, q));
+                    const float2 y = unpack_bf16(u4_get(ky, q));
+                    xr[w] = rope_x(x, y, c);
+                    yr[w] = rope_y(x, y, c);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                out[c] = make_uint4(xr[c], xr[4 + c], xr[8 + c], xr[12 + c]);
+                out[4 + c] = make_uint4(yr[c], yr[4 + c], yr[8 + c], yr[12 + c]);
+            }
+        }
+    }
+}
+
 __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParams P) {
     extern __shared__ unsigned char smem_raw[];
-    const Smem S = ring_setup(P.a, FwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
+    const Smem S = ring_setup(P.a, NCW, FwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the next launch (the next layer) may start its prologue; it waits for
+    // this grid before it touches memory
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == NCW) {
         if (lane == 0) producer(P, S);
     } else {
+        if (P.k_next) rope_next(P, threadIdx.x, NCW * 32);
         consumer(P, S, warp, lane);
     }
 }
@@ -540,8 +593,8 @@ __global__ void __launch_bounds__(kRopeThreads) rope_k_kernel(const __nv_bfloat1
             const float4 t = __ldg(cs + c);
             const float2 x = unpack_bf16(u4_get(xv, c));
             const float2 y = unpack_bf16(u4_get(yv, c));
-            const uint32_t xo = pack_bf16(x.x * t.x - y.x * t.y, x.y * t.z - y.y * t.w);
-            const uint32_t yo = pack_bf16(y.x * t.x + x.x * t.y, y.y * t.z + x.y * t.w);
+            const uint32_t xo = rope_x(x, y, t);
+            const uint32_t yo = rope_y(x, y, t);
             *reinterpret_cast<uint32_t*>(srow + 16 * c + 4 * a) = xo;
             *reinterpret_cast<uint32_t*>(srow + 64 + 16 * c + 4 * a) = yo;
         }
@@ -566,9 +619,13 @@ size_t fwd_mma_workspace(const LayerArgs& a, bool rope) {
     return rope ? (size_t)a.B * a.T * kHkv * kD * sizeof(__nv_bfloat16) : 0;
 }
 
-cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, const void* v,
-                           const float2* rope, void* o, float* lse, void* ws, unsigned* status,
-                           cudaStream_t s) {
+// The attention launch of one layer: khat holds the rotated keys (or the raw
+// keys without RoPE); with k_next set it also rotates the next layer's keys
+// into khat_next.  `after_rope`: the launch directly follows a RoPE pass or
+// an attention launch of this library and may overlap its prologue (PDL).
+cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* khat, const void* v,
+                                 const float2* rope, void* o, float* lse, const void* k_next, void* khat_next,
+                                 unsigned* status, bool pdl, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -583,6 +640,8 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.lse = lse;
     P.status = status;
     P.rope = rope;
+    P.k_next = rope ? static_cast<const __nv_bfloat16*>(k_next) : nullptr;
+    P.khat_next = static_cast<__nv_bfloat16*>(khat_next);
     P.sl2 = a.scale * kLog2e;
     P.inv_sl2 = 1.0f / P.sl2;
     P.ntq = (a.T + TQ - 1) / TQ;
@@ -591,16 +650,6 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.nwt = (a.W + 4 + 15) / 16;
     P.win_region = round1k((unsigned)P.win_rows * ROWB);
     P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
-    const void* khat = k;
-    if (rope) {
-        const unsigned rows = (unsigned)a.B * (unsigned)a.T * kHkv;  // < 2^32: B T < 2^31
-        const unsigned per_block = kRopeThreads / 4;
-        rope_k_kernel<<<(rows + per_block - 1) / per_block, kRopeThreads, 0, s>>>(
-            static_cast<const __nv_bfloat16*>(k), rope, static_cast<__nv_bfloat16*>(ws), rows, (unsigned)a.T);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        count_launch();
-        khat = ws;
-    }
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) ||
         !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows))
         return cudaErrorInvalidValue;
@@ -638,11 +687,31 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = rope ? 1 : 0;
+    cfg.numAttrs = pdl ? 1 : 0;
     e = cudaLaunchKernelEx(&cfg, fwd_mma_kernel, P);
     if (e != cudaSuccess) return e;
     count_launch();
     return cudaSuccess;
+}
+
+cudaError_t launch_rope_k(const LayerArgs& a, const void* k, const float2* rope, void* khat, cudaStream_t s) {
+    const unsigned rows = (unsigned)a.B * (unsigned)a.T * kHkv;  // < 2^32: B T < 2^31
+    const unsigned per_block = kRopeThreads / 4;
+    rope_k_kernel<<<(rows + per_block - 1) / per_block, kRopeThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(k), rope, static_cast<__nv_bfloat16*>(khat), rows, (unsigned)a.T);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
+
+cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, const void* v,
+                           const float2* rope, void* o, float* lse, void* ws, unsigned* status,
+                           cudaStream_t s) {
+    if (rope) {
+        const cudaError_t e = launch_rope_k(a, k, rope, ws, s);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_fwd_attention(a, q, rope ? ws : k, v, rope, o, lse, nullptr, nullptr, status, rope != nullptr, s);
 }
 
 }  // namespace sfa

@@ -17,8 +17,9 @@
 // A parameter struct PP used with these templates provides: kmap_w, vmap_w
 // (window boxes of win_rows rows), kmap_r[RPG], vmap_r[RPG] (rung boxes),
 // a (LayerArgs), rope, status, ntq, ntiles, step_g, step_tq, step_b, win_rows,
-// win_region, and kQMaps (static, >= 1) tile maps qmaps[] of per-query
-// [B][T][8][64] tensors that the query slot carries.
+// win_region, kQMaps (static, >= 1) tile maps qmaps[] of per-query
+// [B][T][8][64] tensors that the query slot carries, and kWinRope (static):
+// whether the window slot also carries the RoPE rows of the tile's queries.
 #pragma once
 
 #include <cuda.h>
@@ -33,8 +34,6 @@ namespace ring {
 using namespace mma;
 
 constexpr int TQ = 28;                 // queries per tile
-constexpr int NCW = 7;                 // consumer warps (2 query pairs each)
-constexpr int NTHREADS = (NCW + 1) * 32;
 constexpr int RPG = 4;                 // rungs per group (one M tile of a query pair)
 constexpr int NGS = 2;                 // group slots
 constexpr int RUNG_ROWS = TQ + 1;      // rows a rung block needs
@@ -114,7 +113,7 @@ struct Smem {
     uint32_t qslot;     // the query slot
     uint32_t win;       // the window slot
     uint32_t rung;      // NGS group slots
-    uint32_t obuf;      // NCW output staging buffers
+    uint32_t obuf;      // the consumer warps' output staging buffers
     int* abort_flag;
     int* kt;            // rungs usable by the window slot's tile
     const SRung* r;     // the kept rungs, by increasing distance
@@ -152,7 +151,7 @@ __device__ __forceinline__ bool load_window(const PP& P, const Smem& S, const Ti
                                             int& kt) {
     if (!mbar_wait(bar_empty_w(S), (wcount & 1) ^ 1, S.abort_flag)) return false;
     const int nq = min(TQ, P.a.T - x.i0);
-    const uint32_t tab_bytes = P.rope ? (uint32_t)nq * TABB : 0u;
+    const uint32_t tab_bytes = (PP::kWinRope && P.rope) ? (uint32_t)nq * TABB : 0u;
     kt = active_rungs(S, P.a.nr, x.i0);
     *S.kt = kt;  // published by the arrive below
     const uint32_t full = bar_full_w(S);
@@ -160,7 +159,7 @@ __device__ __forceinline__ bool load_window(const PP& P, const Smem& S, const Ti
     tma_load_4d(S.win, &P.kmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
     tma_load_4d(S.win + P.win_region, &P.vmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
     // RoPE rows of the tile's query positions (read by the consumers' Q rotation)
-    if (P.rope) bulk_g2s(S.win + 2 * P.win_region, P.rope + (size_t)x.i0 * kPairs, tab_bytes, full);
+    if (tab_bytes) bulk_g2s(S.win + 2 * P.win_region, P.rope + (size_t)x.i0 * kPairs, tab_bytes, full);
     ++wcount;
     return true;
 }
@@ -266,6 +265,17 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
     return v;
 }
 
+// RoPE of two rotation pairs held as bf16 pairs x = (x_m, x_m+1) (dimensions
+// m, m + 1) and y (their partners + D/2), c = (cos_m, sin_m, cos_m+1,
+// sin_m+1): the rotated x and y halves, packed to bf16.  Explicit roundings,
+// so that every kernel that rotates keys produces the same bits.
+__device__ __forceinline__ uint32_t rope_x(float2 x, float2 y, float4 c) {
+    return pack_bf16(__fmaf_rn(x.x, c.x, __fmul_rn(-y.x, c.y)), __fmaf_rn(x.y, c.z, __fmul_rn(-y.y, c.w)));
+}
+__device__ __forceinline__ uint32_t rope_y(float2 x, float2 y, float4 c) {
+    return pack_bf16(__fmaf_rn(y.x, c.x, __fmul_rn(x.x, c.y)), __fmaf_rn(y.y, c.z, __fmul_rn(x.y, c.w)));
+}
+
 __device__ __forceinline__ uint4 lds_u4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -302,9 +312,9 @@ __device__ __forceinline__ uint32_t rung_row(int p, int u, int e, int kind, int 
 // the 1024-byte alignment of the swizzled regions), copies the kept rungs into
 // the header and initialises the barriers: full barriers take one arrival
 // (the producer's expect_tx) plus the copied bytes, empty barriers one
-// arrival per consumer warp.  Ends with a CTA barrier.
-__device__ __forceinline__ Smem ring_setup(const LayerArgs& a, unsigned qslot_bytes, unsigned win_slot_bytes,
-                                           unsigned char* smem_raw) {
+// arrival per consumer warp (ncw of them).  Ends with a CTA barrier.
+__device__ __forceinline__ Smem ring_setup(const LayerArgs& a, int ncw, unsigned qslot_bytes,
+                                           unsigned win_slot_bytes, unsigned char* smem_raw) {
     const uint32_t raw_base = smem_u32(smem_raw);
     const uint32_t base = (raw_base + 1023u) & ~1023u;
     unsigned char* hdr = smem_raw + (base - raw_base);
@@ -326,13 +336,13 @@ __device__ __forceinline__ Smem ring_setup(const LayerArgs& a, unsigned qslot_by
     }
     if (threadIdx.x == 0) {
         mbar_init(bar_full_w(S), 1);
-        mbar_init(bar_empty_w(S), NCW);
+        mbar_init(bar_empty_w(S), ncw);
         for (int i = 0; i < NGS; ++i) {
             mbar_init(bar_full_g(S, i), 1);
-            mbar_init(bar_empty_g(S, i), NCW);
+            mbar_init(bar_empty_g(S, i), ncw);
         }
         mbar_init(bar_full_q(S), 1);
-        mbar_init(bar_empty_q(S), NCW);
+        mbar_init(bar_empty_q(S), ncw);
         *S.abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }

@@ -163,6 +163,35 @@ SFA_API sfa_status sfa_forward(const sfa_params *p, const void *Q, const void *K
                                float *lse, void *workspace, size_t workspace_bytes,
                                unsigned int *status, cudaStream_t stream);
 
+/* ---- forward of several layers ----------------------------------------- */
+
+/* Bytes of device workspace sfa_forward_layers needs for L layers (windows:
+ * host array of L windows, or NULL for p->W in every layer). */
+SFA_API size_t sfa_forward_layers_workspace_size(const sfa_params *p, int L, const int *windows);
+
+/* The forwards of L layers of a model in one call (the paper's model has 16
+ * attention layers, each with its own scalar alpha_l: section 2 "Per-layer
+ * scalar", section 3 "Model and training").  Layer l computes exactly what
+ * sfa_forward computes with *p, alpha = alphas[l] and W = windows[l] (p->W
+ * when windows is NULL) on Q[l], K[l], V[l] into O[l] and lse[l].
+ *   alphas, windows: host arrays of L values; p->alpha is not read;
+ *   Q, K, V, O: host arrays of L device pointers (layouts as sfa_forward);
+ *   lse: host array of L device pointers (entries may be NULL) or NULL;
+ *   workspace: device, 256-byte aligned, >= sfa_forward_layers_workspace_size
+ *     bytes, clobbered; status: as sfa_forward.
+ * When every layer takes the bf16 tensor-core path with RoPE, the call makes
+ * one RoPE launch for layer 0's keys and one attention launch per layer, and
+ * each attention launch also rotates the next layer's keys (two rotated-key
+ * buffers in the workspace, used in turn); otherwise it is L sfa_forward
+ * calls.  Arguments of every layer are checked before anything is launched;
+ * errors as sfa_forward.  Asynchronous on stream. */
+SFA_API sfa_status sfa_forward_layers(const sfa_params *p, int L, const float *alphas,
+                                      const int *windows, const void *const *Q,
+                                      const void *const *K, const void *const *V,
+                                      const float *rope_table, void *const *O, float *const *lse,
+                                      void *workspace, size_t workspace_bytes,
+                                      unsigned int *status, cudaStream_t stream);
+
 /* ---- forward without a caller workspace ------------------------------- */
 
 /* The paper has no counterpart to this entry point: it serves callers that

@@ -187,3 +187,29 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="not built"):
         _lib.load()
+
+
+def test_forward_layers_host_checks(lib):
+    """Argument checks of the multi-layer forward (nothing is launched)."""
+    p = api.Params(2, 64, W=12, alpha=1.0)
+    one = api.Params(2, 64, W=12, alpha=1.0)
+    L = 3
+    win = (ctypes.c_int * L)(12, 12, 12)
+    single = lib.sfa_forward_workspace_size(one.ref())
+    assert lib.sfa_forward_layers_workspace_size(p.ref(), L, win) >= 2 * single
+    assert lib.sfa_forward_layers_workspace_size(p.ref(), 0, win) == 0
+    f32 = api.Params(2, 64, W=12, alpha=1.0, dtype=__import__("torch").float32)
+    assert lib.sfa_forward_layers_workspace_size(f32.ref(), L, None) == 0
+    null = ctypes.c_void_p(0)
+    al = (ctypes.c_float * L)(1.0, 0.8, 1.2)
+    ptrs = (ctypes.c_void_p * L)(16, 16, 16)
+    assert lib.sfa_forward_layers(p.ref(), 0, al, win, ptrs, ptrs, ptrs, null, ptrs, None, null,
+                                  0, null, null) == _lib.SFA_ERR_INVALID_ARG
+    assert lib.sfa_forward_layers(p.ref(), L, None, win, ptrs, ptrs, ptrs, null, ptrs, None, null,
+                                  0, null, null) == _lib.SFA_ERR_INVALID_ARG
+    bad = (ctypes.c_float * L)(1.0, -0.5, 1.2)                      # alpha must be > 0
+    assert lib.sfa_forward_layers(p.ref(), L, bad, win, ptrs, ptrs, ptrs, null, ptrs, None, null,
+                                  0, null, null) == _lib.SFA_ERR_INVALID_ARG
+    mis = (ctypes.c_void_p * L)(16, 24, 16)                          # misaligned layer 1
+    assert lib.sfa_forward_layers(p.ref(), L, al, win, mis, ptrs, ptrs, null, ptrs, None, null,
+                                  0, null, null) == _lib.SFA_ERR_INVALID_ARG
