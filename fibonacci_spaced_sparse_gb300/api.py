@@ -247,9 +247,10 @@ def sfa_backward_workspace_size(B: int, T: int, *, alpha: float, W: int, rungs=F
 
 def sfa_backward(q, k, v, o, dO, lse, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
                  rope_theta: float = 1e4, scale: float = 0.0, workspace=None, status=None,
-                 stream=None):
+                 stream=None, out=None):
     """(dQ, dK, dV, dalpha, dtheta) of the sparse attention; dalpha/dtheta are
-    one-element fp32 device tensors."""
+    one-element fp32 device tensors.  ``out`` may supply the five output
+    tensors (then nothing is allocated here)."""
     _check_qkv(q, k, v)
     B, T = q.shape[0], q.shape[1]
     for name, t in (("o", o), ("dO", dO)):
@@ -261,9 +262,12 @@ def sfa_backward(q, k, v, o, dO, lse, *, alpha: float, W: int, rungs=FIBONACCI_B
     need = int(lib.sfa_backward_workspace_size(p.ref()))
     if workspace is None or workspace.numel() < need:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    da = torch.empty(1, dtype=torch.float32, device=q.device)
-    dth = torch.empty(1, dtype=torch.float32, device=q.device)
+    if out is not None:
+        dq, dk, dv, da, dth = out
+    else:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        da = torch.empty(1, dtype=torch.float32, device=q.device)
+        dth = torch.empty(1, dtype=torch.float32, device=q.device)
     tab = rope_table(T, q.device, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
     st = lib.sfa_backward(p.ref(), _vp(q), _vp(k), _vp(v), _vp(o), _vp(dO), _vp(lse), _vp(tab),
                           _vp(dq), _vp(dk), _vp(dv), _vp(da), _vp(dth), _vp(workspace),

@@ -669,9 +669,18 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
         if (e != cudaSuccess) return e;
         configured_smem[dev & 63] = smem;
     }
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_mma_kernel, NTHREADS, smem);
-    if (e != cudaSuccess) return e;
+    // CTAs per SM for this shared-memory size (looked up once per device and
+    // size, so that no runtime query runs while a stream is being captured)
+    static int occ_per_sm[64];
+    static size_t occ_smem[64];
+    if (occ_smem[dev & 63] != smem) {
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_mma_kernel, NTHREADS, smem);
+        if (e != cudaSuccess) return e;
+        occ_per_sm[dev & 63] = n;
+        occ_smem[dev & 63] = smem;
+    }
+    int per_sm = occ_per_sm[dev & 63];
     if (per_sm < 1) per_sm = 1;
     long long grid = (long long)sms * per_sm;
     if (grid > P.ntiles) grid = P.ntiles;
