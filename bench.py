@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="model-shape",
-                    choices=["model-shape", "extrapolation", "pow2", "train-step", "long-forward"])
+                    choices=["model-shape", "extrapolation", "pow2", "train-step", "long-forward",
+                             "decode"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -63,7 +64,7 @@ def dist_env():
 def workload_of(name):
     from fibonacci_spaced_sparse_gb300 import workloads as w
     return {"model-shape": w.MODEL_SHAPE, "extrapolation": w.EXTRAPOLATION, "pow2": w.POW2,
-            "train-step": w.TRAIN_STEP, "long-forward": w.LONG_FORWARD}[name]
+            "train-step": w.TRAIN_STEP, "long-forward": w.LONG_FORWARD, "decode": w.DECODE}[name]
 
 
 def measured_peak():
@@ -407,6 +408,103 @@ def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
             "d2h_bytes_per_step": d2h, "steps": steps}
 
 
+# ------------------------------------------------------------ decode arm --
+
+def run_decode(args, rank, world, local):
+    """Single-token decode: one step = one new token for each of B sequences
+    through all 16 layers (16 sfa_decode calls, captured once in a CUDA graph
+    and replayed), every layer with its own
+    4096-row key/value cache (seeded N(0, 1) bf16, drawn on the device) and
+    the sequences at seeded positions in the cache's second half.  The
+    caches (8.6 GB) dwarf L2, so every step reads cold rows."""
+    import torch
+    from fibonacci_spaced_sparse_gb300 import api
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload_of("decode")
+    alphas, _ = wl.alphas()
+    L, B, Tc, W = wl.layers, wl.B, wl.T, wl.window(0)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(42 + 1000 * rank)
+    shape = (B, Tc, 2, 64)
+    kc = [torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
+    vc = [torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
+    qs = [torch.randn((B, 8, 64), generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
+    pos = torch.randint(Tc // 2, Tc, (B,), generator=gen, device=dev, dtype=torch.int32)
+    outs = [torch.empty_like(q) for q in qs]
+    lses = [torch.empty((B, 8), dtype=torch.float32, device=dev) for _ in range(L)]
+    api.rope_table(Tc, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def layers(s):
+        for l in range(L):
+            api.sfa_decode(qs[l], kc[l], vc[l], pos, alpha=alphas[l], W=W, out=outs[l], lse=lses[l],
+                           stream=s)
+
+    # the 16 calls of a step are captured once in a CUDA graph (a step is
+    # ~16 short launches; replaying the graph keeps the host out of the timing)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        layers(side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        layers(side)
+
+    def step():
+        graph.replay()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(1, args.steps)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = L * steps  # graph replays: the library's counter sees only the capture
+    ms = start.elapsed_time(stop)
+    # bytes one step must move: every layer's Q and O rows, and the distinct
+    # cache rows (key and value, both kv heads) of each sequence's key list
+    p_host = pos.cpu().numpy()
+    rows = 0
+    for l in range(L):
+        plan = api.rung_plan(T=Tc, W=W, alpha=alphas[l])
+        for i in p_host:
+            used = set(range(max(0, i - W), i + 1))
+            for (_, n, t, c) in plan:
+                if i - c >= 0:
+                    used.add(i - n)
+                    if t > 0:
+                        used.add(i - n - 1)
+            rows += len(used)
+    step_bytes = rows * 2 * 2 * 64 * 2 + L * B * 2 * (8 * 64 * 2)
+    peak, peak_kind = measured_peak()
+    per_layer_s = ms / 1e3 / steps / L
+    achieved = step_bytes / L / per_layer_s / 1e9
+    line = {
+        "metric": "sparse-attn decode tokens/s (one new token per sequence through 16 layers)",
+        "value": B * steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "B": B, "cache_rows": Tc, "W": [W], "layers": L,
+                   "schedule": wl.schedule, "base": wl.base,
+                   "l2": "caches of 8.6 GB, rows read cold each step"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "decode_kernel",
+                     "ideal_bytes_per_launch": step_bytes / L, "avg_launch_us": per_layer_s * 1e6,
+                     "peak_kind": peak_kind},
+        "gpu_launches": launches, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------- reference arm --
 
 def run_reference(args, rank, world):
@@ -462,6 +560,9 @@ def main():
         return
     from fibonacci_spaced_sparse_gb300 import build
     build.build()
+    if args.workload == "decode":
+        run_decode(args, rank, world, local)
+        return
     run_ours(args, rank, world, local)
 
 

@@ -222,6 +222,35 @@ def sfa_forward_layers(qs, ks, vs, *, alphas, W, rungs=FIBONACCI_BASE, rope_thet
     return outs, (lses if need_lse else None)
 
 
+def sfa_decode(q, k_cache, v_cache, positions, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
+               rope_theta: float = 1e4, scale: float = 0.0, need_lse: bool = True, out=None,
+               lse=None, status=None, stream=None):
+    """One new query per sequence over a key/value cache (sfa_decode in
+    include/sfa.h): q [B, 8, 64], caches [B, Tc, 2, 64], positions int32 [B]
+    on the device; returns O [B, 8, 64] and LSE [B, 8]."""
+    if q.dim() != 3 or q.shape[1] != 8 or q.shape[2] != 64 or not q.is_contiguous():
+        raise ValueError(f"q must be a contiguous [B, 8, 64] tensor, got {tuple(q.shape)}")
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if (t.dim() != 4 or t.shape[0] != q.shape[0] or t.shape[2] != 2 or t.shape[3] != 64
+                or not t.is_contiguous() or t.dtype != q.dtype or t.device != q.device):
+            raise ValueError(f"{name} must be a contiguous [B, Tc, 2, 64] tensor like q")
+    if (positions.dtype != torch.int32 or positions.shape != (q.shape[0],)
+            or positions.device != q.device):
+        raise ValueError("positions must be an int32 [B] tensor on q's device")
+    B, Tc = q.shape[0], k_cache.shape[1]
+    o = out if out is not None else torch.empty_like(q)
+    if need_lse and lse is None:
+        lse = torch.empty((B, 8), dtype=torch.float32, device=q.device)
+    p = Params(B, Tc, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
+               dtype=q.dtype)
+    tab = rope_table(Tc, q.device, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
+    st = _lib.load().sfa_decode(p.ref(), _vp(q), _vp(k_cache), _vp(v_cache), _vp(positions),
+                                _vp(tab), _vp(o), _vp(lse if need_lse else None), _vp(status),
+                                _stream(q.device, stream))
+    _lib.check(st, "sfa_decode")
+    return o, (lse if need_lse else None)
+
+
 def sfa_forward_noalloc(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
                         rope_theta: float = 1e4, scale: float = 0.0, out, lse=None, rope=None,
                         status=None, stream=None):

@@ -341,6 +341,21 @@ SFA_API sfa_status sfa_forward_layers(const sfa_params* p, int L, const float* a
     return SFA_OK;
 }
 
+SFA_API sfa_status sfa_decode(const sfa_params* p, const void* Q, const void* Kc, const void* Vc,
+                              const int* positions, const float* rope_table, void* O, float* lse,
+                              unsigned int* status, cudaStream_t stream) {
+    sfa_status st = validate(p);
+    if (st != SFA_OK) return st;
+    if (p->B == 0) return SFA_OK;
+    if (p->T == 0) return SFA_ERR_INVALID_ARG;  // an empty cache holds no position
+    if ((st = check_forward_ptrs(p, Q, Kc, Vc, rope_table, O, lse)) != SFA_OK) return st;
+    if (!positions || (reinterpret_cast<uintptr_t>(positions) & 3u)) return SFA_ERR_INVALID_ARG;
+    LayerArgs a;
+    fill_args(p, &a);
+    return launched(sfa::launch_decode(a, p->T, p->dtype, Q, Kc, Vc, positions, rope_ptr(p, rope_table), O,
+                                       lse, status, stream));
+}
+
 SFA_API size_t sfa_backward_workspace_size(const sfa_params* p) {
     if (validate(p) != SFA_OK) return 0;
     LayerArgs a;

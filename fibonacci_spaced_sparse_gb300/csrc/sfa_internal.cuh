@@ -65,6 +65,10 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
                            const void* dO, const float* lse, const float2* rope, void* dq, void* dk, void* dv,
                            float* dalpha, float* dtheta, void* ws, unsigned* status, cudaStream_t s);
 
+cudaError_t launch_decode(const LayerArgs& a, int Tc, sfa_dtype dt, const void* q, const void* kc,
+                          const void* vc, const int* pos, const float2* rope, void* o, float* lse,
+                          unsigned* status, cudaStream_t s);
+
 size_t bwd_simple_workspace(const LayerArgs& a);
 cudaError_t launch_bwd_simple(const LayerArgs& a, sfa_dtype dt, const void* q, const void* k,
                               const void* v, const void* o, const void* dO, const float* lse,

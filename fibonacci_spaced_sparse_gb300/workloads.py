@@ -59,4 +59,7 @@ TRAIN_STEP = Workload("training step forward+backward", 32, 1024, (12,), "learne
 LONG_FORWARD = Workload("long forward", 2, 16384, (12,), "learned", "fibonacci", 16, "bf16",
                         theta_sigma=0.5)
 
+DECODE = Workload("single-token decode over a 4096-row cache, linear stagger", 256, 4096, (12,),
+                  "linear", "fibonacci", 16, "bf16")
+
 ALL = (TINY_F32, MODEL_SHAPE, EXTRAPOLATION, POW2, TRAIN_STEP, LONG_FORWARD)

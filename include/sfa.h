@@ -216,6 +216,30 @@ SFA_API sfa_status sfa_forward_noalloc(const sfa_params *p, const void *Q, const
                                        const void *V, const float *rope_table, void *O,
                                        float *lse, unsigned int *status, cudaStream_t stream);
 
+/* ---- decode ------------------------------------------------------------ */
+
+/* One new query per sequence over a key/value cache: the attention of query
+ * i = positions[b] of sequence b (section 2 "Attended set"), as sfa_forward
+ * computes it for row (b, i), reading only cache rows 0..i.  This is the
+ * inference workload of the paper's latency comparison between the
+ * interpolated gather and integer offsets (section 3 "Run matrix", section
+ * 4.3).
+ *   p->B: sequences; p->T: cache capacity Tc (>= 1); other fields as
+ *     sfa_forward (the rung plan is made for a sequence of length Tc);
+ *   Q [B][Hq][D]: the new tokens' queries (unrotated when rope_theta > 0);
+ *   Kc, Vc [B][Tc][Hkv][D]: the cache, row i of sequence b holding the new
+ *     token's own key and value (keys unrotated when rope_theta > 0);
+ *   positions: device int32 [B]; a position outside [0, Tc) reads nothing,
+ *     writes zeros to that sequence's outputs and sets SFA_DEVSTAT_BAD_INDEX
+ *     in *status;
+ *   rope_table: >= Tc positions (as sfa_forward); O [B][Hq][D];
+ *   lse [B][Hq] fp32 or NULL.
+ * One launch (fp32 arithmetic for both dtypes); allocates nothing.
+ * Asynchronous on stream. */
+SFA_API sfa_status sfa_decode(const sfa_params *p, const void *Q, const void *Kc,
+                              const void *Vc, const int *positions, const float *rope_table,
+                              void *O, float *lse, unsigned int *status, cudaStream_t stream);
+
 /* ---- backward ---------------------------------------------------------- */
 
 /* Bytes of device workspace sfa_backward needs for these parameters. */

@@ -213,3 +213,20 @@ def test_forward_layers_host_checks(lib):
     mis = (ctypes.c_void_p * L)(16, 24, 16)                          # misaligned layer 1
     assert lib.sfa_forward_layers(p.ref(), L, al, win, mis, ptrs, ptrs, null, ptrs, None, null,
                                   0, null, null) == _lib.SFA_ERR_INVALID_ARG
+
+
+def test_decode_host_checks(lib):
+    """Argument checks of the decode (nothing is launched)."""
+    null = ctypes.c_void_p(0)
+    fake = ctypes.c_void_p(256)
+    p = api.Params(2, 64, W=12, alpha=1.0, rope_theta=0.0)
+    assert lib.sfa_decode(p.ref(), fake, fake, fake, null, null, fake, None, null,
+                          null) == _lib.SFA_ERR_INVALID_ARG           # no positions
+    assert lib.sfa_decode(p.ref(), fake, fake, fake, ctypes.c_void_p(258), null, fake, None, null,
+                          null) == _lib.SFA_ERR_INVALID_ARG           # misaligned positions
+    empty = api.Params(2, 0, W=12, alpha=1.0, rope_theta=0.0)
+    assert lib.sfa_decode(empty.ref(), fake, fake, fake, fake, null, fake, None, null,
+                          null) == _lib.SFA_ERR_INVALID_ARG           # empty cache
+    none = api.Params(0, 64, W=12, alpha=1.0, rope_theta=0.0)
+    assert lib.sfa_decode(none.ref(), null, null, null, null, null, null, None, null,
+                          null) == _lib.SFA_OK                        # nothing to do
