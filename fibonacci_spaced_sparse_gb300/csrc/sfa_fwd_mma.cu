@@ -80,6 +80,7 @@ struct FwdParams {
     unsigned* status;
     const __nv_bfloat16* k_next;  // keys of the next layer (multi-layer forward) or nullptr
     __nv_bfloat16* khat_next;     // where their rotated copy goes
+    unsigned* rope_counter;       // slices of k_next handed out so far (zero at launch)
     float sl2;                 // softmax scale x log2(e)
     float inv_sl2;
     int ntq;                   // query tiles per sequence
@@ -450,6 +451,62 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
     }
 }
 
+// Slices of the next layer's RoPE pass (multi-layer forward): slice n is
+// positions 4n .. 4n + 3 of K_next, rotated into Khat_next in the kdim_of
+// order.  Lane = (position p, head g, stored chunk c): it rotates the pairs
+// m = 8 tig + 2c + {0, 1}, tig = 0..3, which fill stored chunks c (x) and
+// 4 + c (y) of the row.  A warp takes kSlices slices at a time from a counter
+// once its tiles are done -- warps of CTAs with fewer tiles take more -- and
+// issues all their loads before it computes.
+constexpr int kSlices = 4;
+
+__device__ void rope_tail(const FwdParams& P, int lane) {
+    const int npos = P.a.B * P.a.T;
+    const int nslices = (npos + 3) / 4;
+    const int p = lane >> 3, g = (lane >> 2) & 1, c = lane & 3;
+    for (;;) {
+        unsigned first = 0;
+        if (lane == 0) first = atomicAdd(P.rope_counter, (unsigned)kSlices);
+        first = __shfl_sync(kFull, first, 0);
+        if ((int)first >= nslices) break;
+        float4 t[kSlices][4];
+        uint32_t xw[kSlices][4], yw[kSlices][4];
+        size_t row[kSlices];
+        bool ok[kSlices];
+#pragma unroll
+        for (int k = 0; k < kSlices; ++k) {
+            const int pos = 4 * ((int)first + k) + p;
+            ok[k] = pos < npos;
+            const int pc = ok[k] ? pos : npos - 1;
+            row[k] = (size_t)pc * kHkv + g;
+            const unsigned* kw = reinterpret_cast<const unsigned*>(P.k_next + row[k] * kD);
+            const float4* cs = reinterpret_cast<const float4*>(P.rope + (size_t)(pc % P.a.T) * kPairs);
+#pragma unroll
+            for (int tig = 0; tig < 4; ++tig) {
+                // pairs m = 8 tig + 2c + {0, 1}: word 4 tig + c of the row (x), 16 + 4 tig + c (y)
+                t[k][tig] = __ldg(cs + 4 * tig + c);
+                xw[k][tig] = __ldg(kw + 4 * tig + c);
+                yw[k][tig] = __ldg(kw + 16 + 4 * tig + c);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kSlices; ++k) {
+            uint32_t xo[4], yo[4];
+#pragma unroll
+            for (int tig = 0; tig < 4; ++tig) {
+                const float2 x = unpack_bf16(xw[k][tig]), y = unpack_bf16(yw[k][tig]);
+                xo[tig] = rope_x(x, y, t[k][tig]);
+                yo[tig] = rope_y(x, y, t[k][tig]);
+            }
+            if (ok[k]) {
+                uint4* out = reinterpret_cast<uint4*>(P.khat_next + row[k] * kD);
+                out[c] = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+                out[4 + c] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+            }
+        }
+    }
+}
+
 __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) {
     int wcount = 0, gcount = 0, qcount = 0;
     const int u0 = 4 * warp;  // query pairs at tile offsets u0 and u0 + 2
@@ -489,6 +546,11 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
         for (int k = 0; k < 2; ++k) store_unit(P, x, u0 + 2 * k, obuf, L, lane, U[k]);
         x = next_tile(P, x);
     }
+    if (P.k_next) {
+        // the buffer written there was read by the launch before this one
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        rope_tail(P, lane);
+    }
     if (lane == 0) bulk_wait_all();
     return;
 fail:
@@ -496,50 +558,6 @@ fail:
         *S.abort_flag = 1;
         if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
         bulk_wait_all();
-    }
-}
-
-// Khat_next = RoPE(K_next) for the positions (b, j) of this CTA's share
-// (both key/value heads of a position, whole rows, stored in the kdim_of
-// order), done by the consumer warps while the first tile's loads are in
-// flight: the next layer of a multi-layer forward then needs no RoPE launch.
-// The buffer written here was read by the launch before this one.
-__device__ void rope_next(const FwdParams& P, int worker, int nworkers) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int npos = P.a.B * P.a.T;
-    const int per = (npos + (int)gridDim.x - 1) / (int)gridDim.x;
-    const int p0 = (int)blockIdx.x * per, p1 = min(npos, p0 + per);
-    for (int pos = p0 + worker; pos < p1; pos += nworkers) {
-        const int j = pos % P.a.T;
-        const float4* cs = reinterpret_cast<const float4*>(P.rope + (size_t)j * kPairs);  // pairs 2w, 2w + 1
-#pragma unroll 1
-        for (int g = 0; g < kHkv; ++g) {
-            const size_t row = (size_t)pos * kHkv + g;
-            const uint4* kr = reinterpret_cast<const uint4*>(P.k_next + row * kD);
-            uint4* out = reinterpret_cast<uint4*>(P.khat_next + row * kD);
-            // rotated words xr[w] (dimensions 2w, 2w + 1) and yr[w] (+ 32) of
-            // 8-dimension chunk i = w / 4; stored chunk c, word tig holds
-            // dimensions 8 tig + 2c + {0, 1} (+ 32 for c >= 4)
-            uint32_t xr[16], yr[16];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint4 kx = __ldg(kr + i), ky = __ldg(kr + 4 + i);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int w = 4 * i + q;
-                    const float4 c = __ldg(cs + w);
-                    const float2 x = unpack_bf16(u4_get(kx, q));
-                    const float2 y = unpack_bf16(u4_get(ky, q));
-                    xr[w] = rope_x(x, y, c);
-                    yr[w] = rope_y(x, y, c);
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                out[c] = make_uint4(xr[c], xr[4 + c], xr[8 + c], xr[12 + c]);
-                out[4 + c] = make_uint4(yr[c], yr[4 + c], yr[8 + c], yr[12 + c]);
-            }
-        }
     }
 }
 
@@ -553,7 +571,6 @@ __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParam
     if (warp == NCW) {
         if (lane == 0) producer(P, S);
     } else {
-        if (P.k_next) rope_next(P, threadIdx.x, NCW * 32);
         consumer(P, S, warp, lane);
     }
 }
@@ -621,11 +638,11 @@ size_t fwd_mma_workspace(const LayerArgs& a, bool rope) {
 
 // The attention launch of one layer: khat holds the rotated keys (or the raw
 // keys without RoPE); with k_next set it also rotates the next layer's keys
-// into khat_next.  `after_rope`: the launch directly follows a RoPE pass or
+// into khat_next, handing out slices with *rope_counter (zero at launch).  `after_rope`: the launch directly follows a RoPE pass or
 // an attention launch of this library and may overlap its prologue (PDL).
 cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* khat, const void* v,
                                  const float2* rope, void* o, float* lse, const void* k_next, void* khat_next,
-                                 unsigned* status, bool pdl, cudaStream_t s) {
+                                 unsigned* rope_counter, unsigned* status, bool pdl, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -642,6 +659,8 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
     P.rope = rope;
     P.k_next = rope ? static_cast<const __nv_bfloat16*>(k_next) : nullptr;
     P.khat_next = static_cast<__nv_bfloat16*>(khat_next);
+    P.rope_counter = rope_counter;
+    if (P.k_next && !rope_counter) return cudaErrorInvalidValue;
     P.sl2 = a.scale * kLog2e;
     P.inv_sl2 = 1.0f / P.sl2;
     P.ntq = (a.T + TQ - 1) / TQ;
@@ -720,7 +739,8 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
         const cudaError_t e = launch_rope_k(a, k, rope, ws, s);
         if (e != cudaSuccess) return e;
     }
-    return launch_fwd_attention(a, q, rope ? ws : k, v, rope, o, lse, nullptr, nullptr, status, rope != nullptr, s);
+    return launch_fwd_attention(a, q, rope ? ws : k, v, rope, o, lse, nullptr, nullptr, nullptr, status,
+                                rope != nullptr, s);
 }
 
 }  // namespace sfa
