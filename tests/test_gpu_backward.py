@@ -78,3 +78,24 @@ def test_autograd_theta_matches_library():
     _, _, _, _, dth_ref, _ = oracle.backward(*(x[n].double().numpy() for n in ("q", "k", "v", "dO")),
                                               W=8, rungs=FIB, alpha=alpha)
     assert abs(theta.grad.item() - dth_ref) <= 1e-3 * max(1.0, abs(dth_ref))
+
+
+# ------------------------------------------- tensor-core backward edges --
+
+
+@pytest.mark.parametrize("W", [0, 5, 13, 14, 17, 30])
+def test_bf16_window_widths(W):
+    """Window tiles beyond the first (W > 12) and windows narrower than the tile."""
+    run(2, 160, "bf16", alpha=1.13, W=W, layer=4)
+
+
+@pytest.mark.parametrize("T", [2, 29, 33, 97])
+def test_bf16_short_and_ragged_sequences(T):
+    """Sequences shorter than a tile and ragged last tiles (queries past T masked)."""
+    run(3, T, "bf16", alpha=0.77, W=12, layer=6)
+
+
+def test_bf16_without_rope_and_many_rungs():
+    run(2, 200, "bf16", alpha=0.9, W=8, rope_theta=0.0, layer=8)
+    rungs = tuple(range(9, 41))                       # 32 rungs: 8 groups of the ring
+    run(1, 240, "bf16", alpha=1.07, W=8, rungs=rungs, layer=9)

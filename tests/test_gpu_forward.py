@@ -159,7 +159,8 @@ def test_window_widths(W):
 
 
 def test_many_rungs_wrap_the_slot_ring():
-    """32 rungs (the maximum): seven M tiles of five rungs per query tile."""
+    """32 rungs (the maximum): eight groups of four rungs per query tile, so
+    the two group slots of the ring are reused four times each."""
     base = [13 + 7 * k for k in range(32)]
     check_full(2, 300, "bf16", alpha=1.1, W=12, rungs=base, layer=21)
 
