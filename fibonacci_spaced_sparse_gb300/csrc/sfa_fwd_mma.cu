@@ -133,6 +133,7 @@ struct Lane {
                         // quad query 2k + q (before the sequence-start check)
     uint32_t kr[2];     // rung tile of unit k: Khat row offset in a group slot
     uint32_t vr[2];     // rung tile of unit k: V row offset in a group slot
+    uint32_t ki, vi;    // integer-offset rung tile (rows a of the quad): Khat / V row offsets
     uint32_t wk, wv;    // window tile 0: Khat and V row offsets
     uint32_t ob[2];     // output staging: stmatrix row address offsets (jj = 0, 1)
 };
@@ -153,6 +154,9 @@ __device__ __forceinline__ Lane make_lane(int lane, int u0, int W, int win_rows)
     }
     const int rk = (lane & 7) + (((lane >> 3) & 1) << 3);
     const int rv = (lane & 7) + ((lane >> 4) << 3);
+    // integer offsets: M row r is rung r & 3, query e = r >> 2 of the quad, row a
+    L.ki = rung_row(rk & 3, u0, rk >> 2, 1, lane >> 4, false);
+    L.vi = rung_row(rv & 3, u0, rv >> 2, 1, (lane >> 3) & 1, true);
     L.wk = swz_row(min(u0 + rk, win_rows - 1), lane >> 4);
     L.wv = swz_row(min(u0 + rv, win_rows - 1), (lane >> 3) & 1);
     L.wmask = 0u;
@@ -410,6 +414,60 @@ __device__ __forceinline__ void rung_tile(const FwdParams& P, const Smem& S, uin
     }
 }
 
+// The rung M tile when every kept rung has an integer distance (t = 0, so
+// only row a = i - n of a rung is read): row r of the tile is row a of rung
+// k0 + (r & 3) for query e = r >> 2 of the quad, and one tile serves both
+// pairs -- pair 0 (queries 0, 1) reads rows 0..7, pair 1 rows 8..15, so a
+// thread's useful scores are c0, c1 of pair 0 and c2, c3 of pair 1, and the
+// value products run as m16n8k8 on the matching half of the rows.
+__device__ __forceinline__ void rung_tile_int(const FwdParams& P, const Smem& S, uint32_t gslot, int k0, int np,
+                                              int nr, int u0, int i, const Lane& L, Unit* U) {
+    const int lane = threadIdx.x & 31;
+    uint32_t krow = gslot + L.ki, vrow = gslot + L.vi;
+    if (np < RPG) {
+        // rows of absent rung positions read rung 0's block; their entries are masked
+        const int rk = (lane & 7) + (((lane >> 3) & 1) << 3), rv = (lane & 7) + ((lane >> 4) << 3);
+        const int pk = (rk & 3) < np ? (rk & 3) : 0, pv = (rv & 3) < np ? (rv & 3) : 0;
+        krow = gslot + rung_row(pk, u0, rk >> 2, 1, lane >> 4, false);
+        vrow = gslot + rung_row(pv, u0, rv >> 2, 1, (lane >> 3) & 1, true);
+    }
+    // S^T = Khat_rows . Qhat^T for both pairs, one A fragment
+    float c[2][4];
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(krow ^ (uint32_t)(s2 << 5), a0, a1, a2, a3);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            if (s2 == 0)
+                mma16816_z(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+            else
+                mma16816(c[k], a0, a1, a2, a3, U[k].qf[s2][0], U[k].qf[s2][1]);
+        }
+    }
+    const int p = L.g8 & 3;
+    const TC tc = lds_tc(S.tc + (uint32_t)(min(k0 + p, nr - 1) * 8));
+    const int ceil_d = (L.useful && p < np) ? tc.c : kNoRung;
+    uint32_t b[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const bool ok = i + 2 * k + L.q >= ceil_d;
+        float2 sv = k == 0 ? f2(c[0][0], c[0][1]) : f2(c[1][2], c[1][3]);
+        sv.x = ok ? sv.x : -INFINITY;
+        sv.y = ok ? sv.y : -INFINITY;
+        const float2 pe = softmax_step2(P, U[k], sv);
+        b[k] = movm_t(pack_bf16(pe.x, pe.y));
+    }
+    // O^T += V_rows^T . P^T: pair 0 on rows 0..7, pair 1 on rows 8..15
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(vrow ^ (uint32_t)(j << 5), a0, a1, a2, a3);
+        mma1688(U[0].o[j], a0, a1, b[0]);
+        mma1688(U[1].o[j], a2, a3, b[1]);
+    }
+}
+
 // Normalise O^T of the pair at tile offset u and stage it, transposed, in
 // this warp's output buffer (rows (query, head), 128-byte swizzle) for a TMA
 // store; the buffer holds one pair, so the previous store must have read it.
@@ -507,6 +565,7 @@ __device__ void rope_tail(const FwdParams& P, int lane) {
     }
 }
 
+template <bool kInt>
 __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) {
     int wcount = 0, gcount = 0, qcount = 0;
     const int u0 = 4 * warp;  // query pairs at tile offsets u0 and u0 + 2
@@ -536,8 +595,12 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
         for (int k0 = 0; k0 < kt; k0 += RPG) {
             const int slot = gcount & (NGS - 1);
             if (!warp_wait(bar_full_g(S, slot), (gcount / NGS) & 1, S.abort_flag)) goto fail;
-            rung_tile(P, S, S.rung + (uint32_t)slot * kGroupSlotBytes, k0, min(RPG, kt - k0), nr, u0,
-                      x.i0 + u0, L, U);
+            if (kInt)
+                rung_tile_int(P, S, S.rung + (uint32_t)slot * kGroupSlotBytes, k0, min(RPG, kt - k0), nr, u0,
+                              x.i0 + u0, L, U);
+            else
+                rung_tile(P, S, S.rung + (uint32_t)slot * kGroupSlotBytes, k0, min(RPG, kt - k0), nr, u0,
+                          x.i0 + u0, L, U);
             __syncwarp();
             mbar_arrive_if(bar_empty_g(S, slot), lane == 0);
             ++gcount;
@@ -561,6 +624,9 @@ fail:
     }
 }
 
+// kInt: every kept rung has an integer distance (the interpolation weight of
+// row b is zero everywhere), so the rung tiles read rows a only.
+template <bool kInt>
 __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParams P) {
     extern __shared__ unsigned char smem_raw[];
     const Smem S = ring_setup(P.a, NCW, FwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
@@ -571,7 +637,7 @@ __global__ void __maxnreg__(128) fwd_mma_kernel(const __grid_constant__ FwdParam
     if (warp == NCW) {
         if (lane == 0) producer(P, S);
     } else {
-        consumer(P, S, warp, lane);
+        consumer<kInt>(P, S, warp, lane);
     }
 }
 
@@ -648,7 +714,7 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
     if (e != cudaSuccess) return e;
     const int sms = sm_count(dev, &e);
     if (e != cudaSuccess) return e;
-    static size_t configured_smem[64];  // per device: dynamic shared memory already allowed
+    static size_t configured_smem[2][64];  // per variant and device: dynamic shared memory already allowed
     FwdParams P;
     std::memset(&P, 0, sizeof(P));
     P.a = a;
@@ -679,27 +745,31 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
         if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, rows) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, rows))
             return cudaErrorInvalidValue;
     }
+    bool integer_offsets = true;
+    for (int r = 0; r < a.nr; ++r) integer_offsets = integer_offsets && a.r[r].t == 0.f;
+    const auto kernel = integer_offsets ? fwd_mma_kernel<true> : fwd_mma_kernel<false>;
+    const int kidx = integer_offsets ? 1 : 0;
     const size_t smem = 1024 + kHeaderBytes + FwdParams::kQMaps * (size_t)kQTileBytes + (size_t)P.win_slot_bytes +
                         NGS * (size_t)kGroupSlotBytes + NCW * (size_t)kObufBytes;
-    if (configured_smem[dev & 63] < smem) {
-        e = cudaFuncSetAttribute(fwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (configured_smem[kidx][dev & 63] < smem) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(fwd_mma_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
-        configured_smem[dev & 63] = smem;
+        configured_smem[kidx][dev & 63] = smem;
     }
     // CTAs per SM for this shared-memory size (looked up once per device and
     // size, so that no runtime query runs while a stream is being captured)
-    static int occ_per_sm[64];
-    static size_t occ_smem[64];
-    if (occ_smem[dev & 63] != smem) {
+    static int occ_per_sm[2][64];
+    static size_t occ_smem[2][64];
+    if (occ_smem[kidx][dev & 63] != smem) {
         int n = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fwd_mma_kernel, NTHREADS, smem);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, NTHREADS, smem);
         if (e != cudaSuccess) return e;
-        occ_per_sm[dev & 63] = n;
-        occ_smem[dev & 63] = smem;
+        occ_per_sm[kidx][dev & 63] = n;
+        occ_smem[kidx][dev & 63] = smem;
     }
-    int per_sm = occ_per_sm[dev & 63];
+    int per_sm = occ_per_sm[kidx][dev & 63];
     if (per_sm < 1) per_sm = 1;
     long long grid = (long long)sms * per_sm;
     if (grid > P.ntiles) grid = P.ntiles;
@@ -716,7 +786,7 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, fwd_mma_kernel, P);
+    e = cudaLaunchKernelEx(&cfg, kernel, P);
     if (e != cudaSuccess) return e;
     count_launch();
     return cudaSuccess;

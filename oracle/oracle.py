@@ -55,7 +55,7 @@ class _Cfg(ctypes.Structure):
         ("K", ctypes.c_int), ("f", ctypes.POINTER(ctypes.c_double)),
         ("alpha", ctypes.c_double), ("d_fp32", ctypes.c_int),
         ("rope_theta", ctypes.c_double), ("scale", ctypes.c_double),
-        ("nthreads", ctypes.c_int),
+        ("nthreads", ctypes.c_int), ("round_offsets", ctypes.c_int),
     ]
 
 
@@ -94,7 +94,7 @@ def default_threads() -> int:
     return max(1, os.cpu_count() or 1)
 
 
-def _cfg(shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads):
+def _cfg(shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads, round_offsets=False):
     B, T, Hq, D = shape[0], shape[1], shape[2], shape[3]
     f = _f64(rungs)
     cfg = _Cfg()
@@ -106,6 +106,7 @@ def _cfg(shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads):
     cfg.rope_theta = float(rope_theta)
     cfg.scale = float(scale) if scale is not None else 1.0 / math.sqrt(D)
     cfg.nthreads = int(nthreads) if nthreads else default_threads()
+    cfg.round_offsets = 1 if round_offsets else 0
     return cfg, f
 
 
@@ -114,10 +115,11 @@ def _cfg(shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads):
 
 def forward(q, k, v, *, W: int, rungs: Sequence[float], alpha: float,
             rope_theta: float = 1e4, scale: float | None = None,
-            d_fp32: bool = True, nthreads: int | None = None):
+            d_fp32: bool = True, nthreads: int | None = None,
+            round_offsets: bool = False):
     """O [B,T,Hq,D] and LSE [B,T,Hq] of the sparse attention, fp64."""
     q, k, v = _f64(q), _f64(k), _f64(v)
-    cfg, keep = _cfg(q.shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads)
+    cfg, keep = _cfg(q.shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads, round_offsets)
     cfg.Hkv = k.shape[2]
     o = np.zeros(q.shape, dtype=np.float64)
     lse = np.zeros(q.shape[:3], dtype=np.float64)
@@ -130,11 +132,12 @@ def forward(q, k, v, *, W: int, rungs: Sequence[float], alpha: float,
 
 def forward_rows(q, k, v, rows, *, W: int, rungs: Sequence[float], alpha: float,
                  rope_theta: float = 1e4, scale: float | None = None,
-                 d_fp32: bool = True, nthreads: int | None = None):
+                 d_fp32: bool = True, nthreads: int | None = None,
+                 round_offsets: bool = False):
     """O and LSE of the sampled query rows ``rows`` (array of (b, i) pairs)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
-    cfg, keep = _cfg(q.shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads)
+    cfg, keep = _cfg(q.shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads, round_offsets)
     cfg.Hkv = k.shape[2]
     n = rows.shape[0]
     o = np.zeros((n, q.shape[2], q.shape[3]), dtype=np.float64)
@@ -150,10 +153,11 @@ def forward_rows(q, k, v, rows, *, W: int, rungs: Sequence[float], alpha: float,
 
 def backward(q, k, v, dO, *, W: int, rungs: Sequence[float], alpha: float,
              rope_theta: float = 1e4, scale: float | None = None,
-             d_fp32: bool = True, nthreads: int | None = None):
+             d_fp32: bool = True, nthreads: int | None = None,
+             round_offsets: bool = False):
     """(dq, dk, dv, dalpha, dtheta, dt) of L = sum(dO * O), fp64."""
     q, k, v, dO = _f64(q), _f64(k), _f64(v), _f64(dO)
-    cfg, keep = _cfg(q.shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads)
+    cfg, keep = _cfg(q.shape, W, rungs, alpha, d_fp32, rope_theta, scale, nthreads, round_offsets)
     cfg.Hkv = k.shape[2]
     dq = np.zeros(q.shape, dtype=np.float64)
     dk = np.zeros(k.shape, dtype=np.float64)

@@ -59,6 +59,7 @@ typedef struct {
     double rope_theta;      /* <= 0: inputs are used as they are */
     double scale;           /* softmax scale */
     int nthreads;           /* worker threads (>= 1) */
+    int round_offsets;      /* 1: every distance rounded to the nearest integer */
 } oracle_cfg;
 
 /* One attended key: the score and the value read are
@@ -72,16 +73,21 @@ typedef struct {
 
 /* ---------------------------------------------------------------- rungs -- */
 
-/* Distance of rung k ("Attended set": d_k = alpha * f_k). */
+/* Distance of rung k ("Attended set": d_k = alpha * f_k).  With
+ * round_offsets the distance is the nearest integer, halves rounded up (the
+ * static schedules "with integer offsets" of "Implementation notes"). */
 static double rung_distance(const oracle_cfg *c, int k)
 {
+    double d;
     if (c->d_fp32) {
         volatile float a = (float)c->alpha;
         volatile float fk = (float)c->f[k];
-        volatile float d = a * fk;        /* one fp32 multiply, round to nearest */
-        return (double)d;
+        volatile float df = a * fk;       /* one fp32 multiply, round to nearest */
+        d = (double)df;
+    } else {
+        d = c->alpha * c->f[k];
     }
-    return c->alpha * c->f[k];
+    return c->round_offsets ? floor(d + 0.5) : d;
 }
 
 /* The explicit key list of query i ("Attended set").  Returns the count. */
@@ -525,7 +531,8 @@ int oracle_backward(const oracle_cfg *c, const double *q, const double *k, const
                 tot += dt[(size_t)b * Kc + kk];
             if (dt_out)
                 dt_out[kk] = tot;
-            da += c->f[kk] * tot;
+            /* d d_k / d alpha: f_k, or 0 once the distance is rounded */
+            da += (c->round_offsets ? 0.0 : c->f[kk]) * tot;
         }
         *dalpha = da;
         *dtheta = da * (c->alpha - 0.5) * (1.5 - c->alpha);

@@ -177,3 +177,14 @@ def test_integer_offsets_bf16():
 
 def test_without_rope_bf16():
     check_full(2, 160, "bf16", alpha=0.91, W=12, rungs=FIB, rope_theta=0.0)
+
+
+@pytest.mark.parametrize("alpha,W", [(1.0, 0), (1.0, 12), (2.0, 6), (3.0, 20), (1.0, 30)])
+def test_integer_offset_tiles(alpha, W):
+    """Every kept distance an integer (t = 0): the rung tiles that read rows a
+    only (two query pairs per tile), with ragged tiles and partial groups."""
+    check_full(2, 333, "bf16", alpha=alpha, W=W, rungs=FIB, layer=40 + W)
+
+
+def test_integer_offset_tiles_pow2_base():
+    check_full(3, 517, "bf16", alpha=1.0, W=8, rungs=api.pow2_base(517), layer=47)

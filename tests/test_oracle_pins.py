@@ -422,3 +422,59 @@ def test_backward_alpha1_matches_autograd_dense_mask():
     assert np.max(np.abs(dq - dq_ref)) < 1e-11
     assert np.max(np.abs(dk - dk_ref)) < 1e-11
     assert np.max(np.abs(dv - v.grad.numpy())) < 1e-11
+
+
+# ------------------------------------------- rounded (integer) offsets ----
+
+
+def _rounded_dists(alpha, W, base):
+    """fl32(alpha) * fl32(f) rounded to the nearest integer, halves up, kept
+    when beyond the window -- computed here without the oracle."""
+    d = np.float32(alpha) * np.asarray(base, dtype=np.float32)
+    r = np.floor(d.astype(np.float64) + 0.5).astype(int)
+    return sorted(int(x) for x in r if x > W)
+
+
+@pytest.mark.parametrize("alpha,W", [(1.37, 8), (1.0, 6), (1.5, 12), (2.2, 0)])
+def test_round_offsets_equals_dense_mask(alpha, W):
+    """With every distance rounded ("static schedules have integer offsets",
+    section 2 "Implementation notes") the attention is dense attention under
+    the boolean mask of the window and the rounded distances (alpha >= 1
+    keeps the rounded distances distinct)."""
+    T = 200
+    x = _inputs(2, T, layer=15)
+    o, lse = oracle.forward(x["q"], x["k"], x["v"], W=W, rungs=FIB, alpha=alpha,
+                            round_offsets=True)
+    mask = union_mask(T, W, _rounded_dists(alpha, W, FIB))
+    o_ref, lse_ref = sdpa_masked(oracle.rope(x["q"]), oracle.rope(x["k"]), x["v"], mask, 1 / 8)
+    assert np.max(np.abs(o - o_ref)) < 1e-12
+    assert np.max(np.abs(lse - lse_ref)) < 1e-12
+
+
+def test_round_offsets_no_change_at_integer_alpha():
+    x = _inputs(1, 180, layer=16)
+    a = oracle.forward(x["q"], x["k"], x["v"], W=8, rungs=FIB, alpha=1.0, round_offsets=True)
+    b = oracle.forward(x["q"], x["k"], x["v"], W=8, rungs=FIB, alpha=1.0)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_round_offsets_backward_matches_autograd_and_dalpha_is_zero():
+    """Rounded distances do not depend on alpha (zero derivative), and the
+    input gradients are those of dense attention under the rounded mask."""
+    T, W, alpha = 96, 8, 1.29
+    x = _inputs(1, T, layer=17)
+    dq, dk, dv, da, dth, _ = oracle.backward(x["q"], x["k"], x["v"], x["dO"], W=W, rungs=FIB,
+                                             alpha=alpha, round_offsets=True)
+    assert da == 0.0 and dth == 0.0
+    mask = torch.from_numpy(union_mask(T, W, _rounded_dists(alpha, W, FIB)))
+    qh = torch.from_numpy(oracle.rope(x["q"])).requires_grad_(True)
+    kh = torch.from_numpy(oracle.rope(x["k"])).requires_grad_(True)
+    v = torch.from_numpy(x["v"]).requires_grad_(True)
+    q_ = qh.permute(0, 2, 1, 3)
+    k_ = kh.permute(0, 2, 1, 3).repeat_interleave(4, dim=1)
+    v_ = v.permute(0, 2, 1, 3).repeat_interleave(4, dim=1)
+    o = torch.nn.functional.scaled_dot_product_attention(q_, k_, v_, attn_mask=mask, scale=1 / 8)
+    (o.permute(0, 2, 1, 3) * torch.from_numpy(x["dO"])).sum().backward()
+    assert np.max(np.abs(dq - oracle.rope(qh.grad.numpy(), inverse=True))) < 1e-11
+    assert np.max(np.abs(dk - oracle.rope(kh.grad.numpy(), inverse=True))) < 1e-11
+    assert np.max(np.abs(dv - v.grad.numpy())) < 1e-11
