@@ -31,6 +31,7 @@ class SfaParams(ctypes.Structure):
         ("rungs", ctypes.POINTER(ctypes.c_float)),
         ("alpha", ctypes.c_float), ("rope_theta", ctypes.c_float),
         ("scale", ctypes.c_float), ("dtype", ctypes.c_int),
+        ("round_offsets", ctypes.c_int),
     ]
 
 

@@ -46,7 +46,7 @@ class Params:
     """An sfa_params struct plus the host rung array it points to."""
 
     def __init__(self, B, T, *, W, alpha, rungs=FIBONACCI_BASE, rope_theta=1e4, scale=0.0,
-                 dtype=torch.bfloat16, Hq=8, Hkv=2, D=64):
+                 dtype=torch.bfloat16, Hq=8, Hkv=2, D=64, round_offsets=False):
         self._rungs = (ctypes.c_float * max(1, len(rungs)))(*[float(f) for f in rungs])
         p = _lib.SfaParams()
         p.B, p.T, p.Hq, p.Hkv, p.D = int(B), int(T), int(Hq), int(Hkv), int(D)
@@ -58,6 +58,7 @@ class Params:
         if dtype not in _DTYPES:
             raise TypeError(f"unsupported dtype {dtype}")
         p.dtype = _DTYPES[dtype]
+        p.round_offsets = 1 if round_offsets else 0
         self.struct = p
 
     def ref(self):
@@ -84,10 +85,11 @@ def alpha_schedule(kind: str, L: int = 16, S: int = 7, thetas: Sequence[float] |
     return [float(x) for x in out]
 
 
-def rung_plan(*, T: int, W: int, alpha: float, rungs=FIBONACCI_BASE, B: int = 1):
+def rung_plan(*, T: int, W: int, alpha: float, rungs=FIBONACCI_BASE, B: int = 1,
+              round_offsets: bool = False):
     """The rungs the kernels use: list of (index, floor d, t, ceil d)."""
     lib = _lib.load()
-    p = Params(B, T, W=W, alpha=alpha, rungs=rungs)
+    p = Params(B, T, W=W, alpha=alpha, rungs=rungs, round_offsets=round_offsets)
     K = max(1, len(rungs))
     n = ctypes.c_int(0)
     idx, fl, ce = (ctypes.c_int * K)(), (ctypes.c_int * K)(), (ctypes.c_int * K)()
@@ -159,7 +161,7 @@ def _workspace(device, nbytes: int) -> torch.Tensor:
 
 def sfa_forward(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE, rope_theta: float = 1e4,
                 scale: float = 0.0, need_lse: bool = True, out=None, lse=None, status=None,
-                workspace=None, stream=None):
+                workspace=None, stream=None, round_offsets: bool = False):
     """O (and LSE) of the sparse attention for one layer; see include/sfa.h."""
     _check_qkv(q, k, v)
     B, T = q.shape[0], q.shape[1]
@@ -167,7 +169,7 @@ def sfa_forward(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE, rope_the
     if need_lse and lse is None:
         lse = torch.empty((B, T, 8), dtype=torch.float32, device=q.device)
     p = Params(B, T, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
-               dtype=q.dtype)
+               dtype=q.dtype, round_offsets=round_offsets)
     lib = _lib.load()
     need = int(lib.sfa_forward_workspace_size(p.ref()))
     if workspace is None or workspace.numel() < need:
@@ -187,7 +189,7 @@ def _ptrs(ts) -> ctypes.Array:
 
 def sfa_forward_layers(qs, ks, vs, *, alphas, W, rungs=FIBONACCI_BASE, rope_theta: float = 1e4,
                        scale: float = 0.0, need_lse: bool = True, outs=None, lses=None,
-                       status=None, workspace=None, stream=None):
+                       status=None, workspace=None, stream=None, round_offsets: bool = False):
     """The forwards of L layers in one call (sfa_forward_layers in
     include/sfa.h): qs, ks, vs are lists of per-layer tensors, alphas the L
     per-layer scalars, W one window or a list of L windows."""
@@ -205,7 +207,7 @@ def sfa_forward_layers(qs, ks, vs, *, alphas, W, rungs=FIBONACCI_BASE, rope_thet
         lses = [torch.empty((B, T, 8), dtype=torch.float32, device=dev) for _ in range(L)]
     windows = [int(W)] * L if isinstance(W, int) else [int(w) for w in W]
     p = Params(B, T, W=windows[0], alpha=alphas[0], rungs=rungs, rope_theta=rope_theta,
-               scale=scale, dtype=qs[0].dtype)
+               scale=scale, dtype=qs[0].dtype, round_offsets=round_offsets)
     win = (ctypes.c_int * L)(*windows)
     al = (ctypes.c_float * L)(*[float(a) for a in alphas])
     lib = _lib.load()
@@ -224,7 +226,7 @@ def sfa_forward_layers(qs, ks, vs, *, alphas, W, rungs=FIBONACCI_BASE, rope_thet
 
 def sfa_decode(q, k_cache, v_cache, positions, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
                rope_theta: float = 1e4, scale: float = 0.0, need_lse: bool = True, out=None,
-               lse=None, status=None, stream=None):
+               lse=None, status=None, stream=None, round_offsets: bool = False):
     """One new query per sequence over a key/value cache (sfa_decode in
     include/sfa.h): q [B, 8, 64], caches [B, Tc, 2, 64], positions int32 [B]
     on the device; returns O [B, 8, 64] and LSE [B, 8]."""
@@ -242,7 +244,7 @@ def sfa_decode(q, k_cache, v_cache, positions, *, alpha: float, W: int, rungs=FI
     if need_lse and lse is None:
         lse = torch.empty((B, 8), dtype=torch.float32, device=q.device)
     p = Params(B, Tc, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
-               dtype=q.dtype)
+               dtype=q.dtype, round_offsets=round_offsets)
     tab = rope_table(Tc, q.device, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
     st = _lib.load().sfa_decode(p.ref(), _vp(q), _vp(k_cache), _vp(v_cache), _vp(positions),
                                 _vp(tab), _vp(o), _vp(lse if need_lse else None), _vp(status),
@@ -269,14 +271,14 @@ def sfa_forward_noalloc(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
 
 
 def sfa_backward_workspace_size(B: int, T: int, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
-                                dtype=torch.bfloat16) -> int:
-    p = Params(B, T, W=W, alpha=alpha, rungs=rungs, dtype=dtype)
+                                dtype=torch.bfloat16, round_offsets: bool = False) -> int:
+    p = Params(B, T, W=W, alpha=alpha, rungs=rungs, dtype=dtype, round_offsets=round_offsets)
     return int(_lib.load().sfa_backward_workspace_size(p.ref()))
 
 
 def sfa_backward(q, k, v, o, dO, lse, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
                  rope_theta: float = 1e4, scale: float = 0.0, workspace=None, status=None,
-                 stream=None, out=None):
+                 stream=None, out=None, round_offsets: bool = False):
     """(dQ, dK, dV, dalpha, dtheta) of the sparse attention; dalpha/dtheta are
     one-element fp32 device tensors.  ``out`` may supply the five output
     tensors (then nothing is allocated here)."""
@@ -286,7 +288,7 @@ def sfa_backward(q, k, v, o, dO, lse, *, alpha: float, W: int, rungs=FIBONACCI_B
         if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
             raise ValueError(f"{name} must match q")
     p = Params(B, T, W=W, alpha=alpha, rungs=rungs, rope_theta=rope_theta, scale=scale,
-               dtype=q.dtype)
+               dtype=q.dtype, round_offsets=round_offsets)
     lib = _lib.load()
     need = int(lib.sfa_backward_workspace_size(p.ref()))
     if workspace is None or workspace.numel() < need:

@@ -42,6 +42,7 @@ sfa_status validate(const sfa_params* p) {
     if (!std::isfinite(p->rope_theta) || !std::isfinite(p->scale) || p->scale < 0.f)
         return SFA_ERR_INVALID_ARG;
     if (p->dtype != SFA_F32 && p->dtype != SFA_BF16) return SFA_ERR_INVALID_ARG;
+    if (p->round_offsets != 0 && p->round_offsets != 1) return SFA_ERR_INVALID_ARG;
     if (p->Hq != sfa::kHq || p->Hkv != sfa::kHkv || p->D != sfa::kD) return SFA_ERR_UNSUPPORTED;
     if (p->T > kMaxT || (long long)p->B * p->T > 0x7fffffffLL) return SFA_ERR_UNSUPPORTED;
     return SFA_OK;
@@ -55,7 +56,9 @@ int rung_plan(const sfa_params* p, Rung* out) {
     int n = 0;
     for (int k = 0; k < p->K; ++k) {
         volatile float d = p->alpha * p->rungs[k];
-        const float dv = d;
+        // rounded mode: the nearest integer, halves up (computed in double on
+        // the fp32 product)
+        const float dv = p->round_offsets ? (float)std::floor((double)d + 0.5) : (float)d;
         if (!(dv > (float)p->W)) continue;
         if (dv >= (float)p->T) continue;  // ceil(d) >= T: masked for all i < T
         const float fl = std::floor(dv);
@@ -65,7 +68,7 @@ int rung_plan(const sfa_params* p, Rung* out) {
         r.n = (int)fl;
         r.t = dv - fl;  // exact: fl and dv share the exponent range
         r.c = (int)ce;
-        r.f = p->rungs[k];
+        r.f = p->round_offsets ? 0.f : p->rungs[k];  // d d / d alpha (zero once rounded)
         r.index = k;
         // insertion by increasing distance (stable): the rungs a query tile can
         // use are then a prefix of the list

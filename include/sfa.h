@@ -85,6 +85,11 @@ typedef struct {
     float rope_theta;  /* RoPE base (1e4 in the paper); <= 0: inputs already rotated */
     float scale;       /* softmax scale; 0 selects 1/sqrt(D) */
     sfa_dtype dtype;   /* element type of Q, K, V, O, dO, dQ, dK, dV */
+    int round_offsets; /* 0: d_k as computed (interpolated gather); 1: every d_k
+                          rounded to the nearest integer, halves up (the static
+                          schedules "with integer offsets", section 2
+                          "Implementation notes"): one row per rung, and
+                          dL/dalpha = 0 */
 } sfa_params;
 
 /* Library version, (major << 16) | minor. */
@@ -121,7 +126,9 @@ SFA_API sfa_status sfa_alpha_schedule(sfa_schedule kind, int L, int S,
 /* The rungs the kernels will use for this layer, by increasing distance: for
  * every base offset with d_k = fl32(alpha) * fl32(f_k) > W and
  * ceil(d_k) <= T - 1 (rungs beyond that are masked for every query) it
- * reports the table index, floor(d_k), t = d_k - floor(d_k) and ceil(d_k).
+ * reports the table index, floor(d_k), t = d_k - floor(d_k) and ceil(d_k)
+ * (with p->round_offsets, d_k is first rounded to the nearest integer, halves
+ * up, so that t = 0 and floor = ceil).
  * Arrays are host arrays of at least p->K entries; *n_active receives the
  * count.  This is the same routine sfa_forward and sfa_backward use. */
 SFA_API sfa_status sfa_rung_plan(const sfa_params *p, int *n_active, int *index,

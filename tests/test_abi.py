@@ -116,6 +116,27 @@ def test_rung_plan_boundaries(lib):
     assert set(api.pow2_base(4096)) >= {1024, 2048}
 
 
+def test_rung_plan_rounded(lib):
+    """round_offsets: integer distances (t = 0), halves up, computed on the fp32
+    product alpha * f_k; rounded distances inside the window are dropped."""
+    plan = api.rung_plan(T=1024, W=3, alpha=0.5, round_offsets=True)
+    # d = 1.5, 2.5, 4, 6.5, 10.5, ... -> 2, 3 (inside W = 3), 4, 7, 11, ...
+    assert [(r[1], r[2], r[3]) for r in plan[:3]] == [(4, 0.0, 4), (7, 0.0, 7), (11, 0.0, 11)]
+    assert all(r[2] == 0.0 and r[1] == r[3] for r in plan)
+    # fp32(2.1) * 55 is just below 115.5: rounds down to 115, not up to 116
+    assert np.float32(2.1) * np.float32(55) < np.float32(115.5)
+    assert api.rung_plan(T=256, W=0, alpha=2.1, rungs=[55], round_offsets=True) == \
+        [(0, 115, 0.0, 115)]
+    # 10.96 rounds to 11 = W: dropped, though the interpolated rung is kept at W = 10
+    assert api.rung_plan(T=64, W=11, alpha=1.37, rungs=[8], round_offsets=True) == []
+    assert len(api.rung_plan(T=64, W=10, alpha=1.37, rungs=[8])) == 1
+    p = api.Params(1, 16, W=2, alpha=1.0)
+    p.struct.round_offsets = 2
+    n = ctypes.c_int(0)
+    assert lib.sfa_rung_plan(p.ref(), ctypes.byref(n), None, None, None, None) == \
+        _lib.SFA_ERR_INVALID_ARG
+
+
 def _params(**kw):
     d = dict(W=12, alpha=1.0)
     d.update(kw)
