@@ -253,6 +253,30 @@ def sfa_decode(q, k_cache, v_cache, positions, *, alpha: float, W: int, rungs=FI
     return o, (lse if need_lse else None)
 
 
+def sfa_qkv_rope(x, w_qkv, *, rope_theta: float = 1e4, out=None, status=None, stream=None):
+    """The fused front end (sfa_qkv_rope in include/sfa.h): x [B, T, d_model]
+    and w_qkv [768, d_model] bf16 on the device; returns (qhat [B, T, 8, 64],
+    khat [B, T, 2, 64], v [B, T, 2, 64]) with RoPE applied to qhat and khat,
+    ready for sfa_forward(..., rope_theta=0)."""
+    if x.dim() != 3 or x.dtype != torch.bfloat16 or not x.is_contiguous():
+        raise ValueError(f"x must be a contiguous bf16 [B, T, d_model] tensor, got {tuple(x.shape)}")
+    B, T, dm = x.shape
+    if (w_qkv.shape != (768, dm) or w_qkv.dtype != torch.bfloat16 or not w_qkv.is_contiguous()
+            or w_qkv.device != x.device):
+        raise ValueError(f"w_qkv must be a contiguous bf16 [768, {dm}] tensor on x's device")
+    if out is None:
+        out = (torch.empty((B, T, 8, 64), dtype=x.dtype, device=x.device),
+               torch.empty((B, T, 2, 64), dtype=x.dtype, device=x.device),
+               torch.empty((B, T, 2, 64), dtype=x.dtype, device=x.device))
+    qh, kh, v = out
+    p = Params(B, T, W=0, alpha=1.0, rope_theta=rope_theta, dtype=x.dtype)
+    tab = rope_table(T, x.device, rope_theta=rope_theta, stream=stream) if rope_theta > 0 else None
+    st = _lib.load().sfa_qkv_rope(p.ref(), int(dm), _vp(x), _vp(w_qkv), _vp(tab), _vp(qh), _vp(kh),
+                                  _vp(v), _vp(status), _stream(x.device, stream))
+    _lib.check(st, "sfa_qkv_rope")
+    return qh, kh, v
+
+
 def sfa_forward_noalloc(q, k, v, *, alpha: float, W: int, rungs=FIBONACCI_BASE,
                         rope_theta: float = 1e4, scale: float = 0.0, out, lse=None, rope=None,
                         status=None, stream=None):

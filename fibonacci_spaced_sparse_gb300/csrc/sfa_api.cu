@@ -363,6 +363,23 @@ SFA_API sfa_status sfa_decode(const sfa_params* p, const void* Q, const void* Kc
                                        lse, status, stream));
 }
 
+SFA_API sfa_status sfa_qkv_rope(const sfa_params* p, int d_model, const void* X, const void* Wqkv,
+                                const float* rope_table, void* Qhat, void* Khat, void* V,
+                                unsigned int* status, cudaStream_t stream) {
+    sfa_status st = validate(p);
+    if (st != SFA_OK) return st;
+    if (p->dtype != SFA_BF16) return SFA_ERR_UNSUPPORTED;
+    if (d_model < 64 || d_model > 16384 || d_model % 64 != 0) return SFA_ERR_INVALID_ARG;
+    const long long M = (long long)p->B * p->T;
+    if (M == 0) return SFA_OK;
+    if (!X || !Wqkv || !Qhat || !Khat || !V || !aligned16(X) || !aligned16(Wqkv) || !aligned16(Qhat) ||
+        !aligned16(Khat) || !aligned16(V))
+        return SFA_ERR_INVALID_ARG;
+    if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
+    return launched(sfa::launch_qkv_rope((int)M, p->T, d_model, X, Wqkv, rope_ptr(p, rope_table), Qhat, Khat,
+                                         V, status, stream));
+}
+
 SFA_API size_t sfa_backward_workspace_size(const sfa_params* p) {
     if (validate(p) != SFA_OK) return 0;
     LayerArgs a;

@@ -1,0 +1,346 @@
+// sfa_qkv.cu -- the front end of an attention layer: the QKV projection
+// [Q | K | V] = X . Wqkv^T on the 5th-generation tensor cores, with RoPE
+// applied to Q and K in the epilogue, writing the bf16 tensors the sparse
+// attention reads.
+//
+// "Depth-Staggered Fibonacci Spacing for Sparse Attention" (arXiv 2606.28560),
+// section 2 "Attended set": RoPE (theta = 1e4) is applied to queries and keys
+// at their true positions before any key row is gathered; section 3 "Model
+// and training": d_model 512, 8 query heads and 2 key/value heads of
+// dimension 64, so Wqkv has (8 + 2 + 2) x 64 = 768 rows.  With RoPE done here
+// the attention runs on the rotated tensors with its own rotation off.
+//
+// One CTA computes a tile of BM = 128 tokens x BN = 256 output features (four
+// heads) over the whole d_model:
+//   warp 0 (one lane): TMA loads of the X and Wqkv k-blocks (64 columns,
+//                      128-byte swizzle) into a two-stage mbarrier ring;
+//   warp 1:            allocates 256 TMEM columns; one lane issues
+//                      tcgen05.mma (M = 128, N = 256, K = 16, bf16 -> fp32)
+//                      with the fp32 tile accumulating in TMEM, and releases
+//                      each stage with tcgen05.commit;
+//   warps 2..5:        the epilogue: each thread owns one token row (TMEM lane),
+//                      reads a head's 64 columns with tcgen05.ld, rotates the
+//                      pairs (m, m + 32) by the angle of the token's position
+//                      (from the fp64-built table of sfa_rope_table) and
+//                      stores the head row in bf16.
+// Two CTAs fit on an SM (96 KB of stages each, 256 TMEM columns each), so one
+// CTA's epilogue overlaps the other's main loop.  Every wait is bounded; a
+// timeout sets SFA_DEVSTAT_WAIT_TIMEOUT and the CTA leaves without writing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "sfa_internal.cuh"
+#include "sfa_mma.cuh"
+
+namespace sfa {
+
+namespace {
+
+using namespace mma;
+
+constexpr int BM = 128;                 // tokens per tile (TMEM lanes)
+constexpr int BN = 256;                 // output features per tile (TMEM columns)
+constexpr int BK = 64;                  // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 2;
+constexpr int UMMA_K = 16;
+constexpr uint32_t kABytes = BM * BK * 2;  // 16 KB
+constexpr uint32_t kBBytes = BN * BK * 2;  // 32 KB
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr int kThreads = 192;           // 6 warps
+constexpr int kQkvRows = kHq * kD + 2 * kHkv * kD;  // 768 output features
+constexpr int kNTiles = kQkvRows / BN;              // 3
+constexpr uint32_t kTmemCols = BN;
+// header: full[STAGES], empty[STAGES], tmem_full barriers, the TMEM address, the abort flag
+constexpr uint32_t kHdrBytes = 1024;
+constexpr size_t kSmemBytes = 1024 + kHdrBytes + STAGES * (size_t)kStageBytes;
+
+static_assert(kQkvRows % BN == 0, "the projection splits into whole tiles");
+static_assert(BN % kD == 0 && (kHq * kD) % BN == 0, "tiles hold whole heads; Q tiles hold only Q heads");
+
+struct QkvParams {
+    CUtensorMap xmap;   // X [M][dm] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap wmap;   // Wqkv [768][dm] bf16, box 64 x 256, 128-byte swizzle
+    __nv_bfloat16* q;   // [M][8][64]
+    __nv_bfloat16* k;   // [M][2][64]
+    __nv_bfloat16* v;   // [M][2][64]
+    const float2* rope; // [T][32] (cos, sin) or nullptr (no rotation)
+    unsigned* status;
+    int M, T, nkb;      // tokens, positions per sequence, k-blocks (dm / 64)
+};
+
+// ------------------------------------------------------------ tcgen05 PTX
+
+// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte
+// swizzle that TMA writes: start address >> 4 (bits 0-13), leading-dimension
+// offset (unused for this layout, 1), stride between 8-row core-matrix groups
+// = 1024 bytes (bits 32-45), the fixed descriptor version 1 (bits 46-48),
+// layout 2 = 128-byte swizzle (bits 61-63).  Tile bases are 1024-byte
+// aligned; a K step of 16 elements advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
+// B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
+// bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+// The mbarrier gets one arrival once every tcgen05.mma issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&r)[32]) {
+    uint32_t u[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
+          "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]),
+          "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]),
+          "=r"(u[30]), "=r"(u[31])
+        : "r"(taddr));
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = __uint_as_float(u[j]);
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// ------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kThreads) qkv_rope_kernel(const __grid_constant__ QkvParams P) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char* hdr = smem_raw + (base - raw);
+    const uint32_t bar_full = base, bar_empty = base + 8 * STAGES, bar_tmem = base + 16 * STAGES;
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(hdr + 16 * STAGES + 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(hdr + 16 * STAGES + 16);
+    const uint32_t stages = base + kHdrBytes;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x / kNTiles, nt = blockIdx.x % kNTiles;
+    const int m0 = mt * BM, n0 = nt * BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        mbar_init(bar_tmem, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(const_cast<uint32_t*>(tmem_slot))),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < P.nkb; ++kb) {
+                const int s = kb % STAGES;
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t a = stages + (uint32_t)s * kStageBytes;
+                mbar_arrive_expect_tx(bar_full + 8 * s, kStageBytes);
+                tma_load_2d(a, &P.xmap, kb * BK, m0, bar_full + 8 * s);
+                tma_load_2d(a + kABytes, &P.wmap, kb * BK, n0, bar_full + 8 * s);
+                ++issued;
+            }
+            // Nothing may land in this CTA's shared memory after it leaves: wait
+            // for the MMA's release of the last use of every stage (its
+            // tcgen05.commit arrival), or, once a wait has failed, for the
+            // copies themselves.
+            const bool clean = *abort_flag == 0;
+            for (int kb = max(0, issued - STAGES); kb < issued; ++kb) {
+                const uint32_t ph = (uint32_t)(kb / STAGES) & 1u;
+                if (!clean || !mbar_wait(bar_empty + 8 * (kb % STAGES), ph, nullptr))
+                    (void)mbar_wait(bar_full + 8 * (kb % STAGES), ph, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int done = 0;
+            for (int kb = 0; kb < P.nkb; ++kb) {
+                const int s = kb % STAGES;
+                if (!mbar_wait(bar_full + 8 * s, (uint32_t)(kb / STAGES) & 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a = stages + (uint32_t)s * kStageBytes;
+                const uint64_t ad = umma_desc(a), bd = umma_desc(a + kABytes);
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k)
+                    tc_mma(tmem, ad + (uint64_t)(k * UMMA_K * 2 / 16), bd + (uint64_t)(k * UMMA_K * 2 / 16),
+                           (kb | k) != 0);
+                tc_commit(bar_empty + 8 * s);  // the stage is free once these have read it
+                ++done;
+            }
+            (void)done;
+            // the accumulator is complete once every MMA above has (also when
+            // none was issued or the loop stopped early)
+            tc_commit(bar_tmem);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31
+        const int lb = 32 * (warp & 3);
+        const int row = lb + lane, m = m0 + row;
+        const bool ok = mbar_wait(bar_tmem, 0, nullptr) && *abort_flag == 0;
+        tc_fence_after();
+        if (ok) {
+            const int pos = m < P.M ? m % P.T : 0;
+#pragma unroll 1
+            for (int h = 0; h < BN / kD; ++h) {
+                float x[32], y[32];
+                const uint32_t ta = tmem + ((uint32_t)lb << 16) + (uint32_t)(h * kD);
+                tc_ld32(ta, x);
+                tc_ld32(ta + kPairs, y);
+                tc_wait_ld();
+                const int hh = (n0 + h * kD) / kD;  // global head row block: Q 0..7, K 8..9, V 10..11
+                __nv_bfloat16* dst;
+                bool rot = P.rope != nullptr;
+                if (hh < kHq) {
+                    dst = P.q + ((size_t)m * kHq + hh) * kD;
+                } else if (hh < kHq + kHkv) {
+                    dst = P.k + ((size_t)m * kHkv + (hh - kHq)) * kD;
+                } else {
+                    dst = P.v + ((size_t)m * kHkv + (hh - kHq - kHkv)) * kD;
+                    rot = false;
+                }
+                if (rot) {
+                    const float4* cs = reinterpret_cast<const float4*>(P.rope + (size_t)pos * kPairs);
+#pragma unroll
+                    for (int j2 = 0; j2 < kPairs / 2; ++j2) {
+                        const float4 c = __ldg(cs + j2);  // pairs 2 j2, 2 j2 + 1
+                        const float x0 = x[2 * j2], y0 = y[2 * j2], x1 = x[2 * j2 + 1], y1 = y[2 * j2 + 1];
+                        x[2 * j2] = __fmaf_rn(x0, c.x, __fmul_rn(-y0, c.y));
+                        y[2 * j2] = __fmaf_rn(y0, c.x, __fmul_rn(x0, c.y));
+                        x[2 * j2 + 1] = __fmaf_rn(x1, c.z, __fmul_rn(-y1, c.w));
+                        y[2 * j2 + 1] = __fmaf_rn(y1, c.z, __fmul_rn(x1, c.w));
+                    }
+                }
+                if (m < P.M) {
+                    uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        out[c] = make_uint4(pack_bf16(x[8 * c], x[8 * c + 1]), pack_bf16(x[8 * c + 2], x[8 * c + 3]),
+                                            pack_bf16(x[8 * c + 4], x[8 * c + 5]),
+                                            pack_bf16(x[8 * c + 6], x[8 * c + 7]));
+                        out[4 + c] = make_uint4(pack_bf16(y[8 * c], y[8 * c + 1]), pack_bf16(y[8 * c + 2], y[8 * c + 3]),
+                                                pack_bf16(y[8 * c + 4], y[8 * c + 5]),
+                                                pack_bf16(y[8 * c + 6], y[8 * c + 7]));
+                    }
+                }
+            }
+        } else if (lane == 0 && warp == 2 && P.status) {
+            atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// 2-D map over a row-major bf16 matrix [rows][cols], box of 64 columns x
+// box_rows rows, 128-byte swizzle, zero fill outside.
+bool encode_matrix(CUtensorMap* m, const void* base, int rows, int cols, int box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+size_t qkv_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_qkv_rope(int M, int T, int dm, const void* x, const void* w, const float2* rope, void* q,
+                            void* k, void* v, unsigned* status, cudaStream_t s) {
+    if (M <= 0) return cudaSuccess;
+    QkvParams P;
+    std::memset(&P, 0, sizeof(P));
+    if (!encode_matrix(&P.xmap, x, M, dm, BM) || !encode_matrix(&P.wmap, w, kQkvRows, dm, BN))
+        return cudaErrorInvalidValue;
+    P.q = static_cast<__nv_bfloat16*>(q);
+    P.k = static_cast<__nv_bfloat16*>(k);
+    P.v = static_cast<__nv_bfloat16*>(v);
+    P.rope = rope;
+    P.status = status;
+    P.M = M;
+    P.T = T;
+    P.nkb = dm / BK;
+    static bool configured[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (!configured[dev & 63]) {
+        e = cudaFuncSetAttribute(qkv_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev & 63] = true;
+    }
+    const long long tiles = (long long)((M + BM - 1) / BM) * kNTiles;
+    qkv_rope_kernel<<<(unsigned)tiles, kThreads, kSmemBytes, s>>>(P);
+    e = cudaGetLastError();
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
+
+}  // namespace sfa

@@ -12,7 +12,7 @@ from __future__ import annotations
 
 import torch
 
-_STREAMS = {"q": 0, "k": 1, "v": 2, "dO": 3, "theta": 4}
+_STREAMS = {"q": 0, "k": 1, "v": 2, "dO": 3, "theta": 4, "x": 5, "w": 6}
 
 
 def _gen(seed: int, layer: int, stream: str) -> torch.Generator:
@@ -46,3 +46,14 @@ def thetas(L: int, sigma: float, *, seed: int = 42) -> list:
     g = _gen(seed, 0, "theta")
     x = torch.randn((L,), generator=g, dtype=torch.float64) * float(sigma)
     return [float(t) for t in x]
+
+
+def hidden_and_weight(B: int, T: int, d_model: int = 512, rows: int = 768, *,
+                      dtype=torch.bfloat16, seed: int = 42, layer: int = 0):
+    """Inputs of the QKV front end: hidden states X [B,T,d_model] ~ N(0, 1) and
+    a projection weight [rows, d_model] ~ N(0, 1/d_model) (so that the
+    projections are of unit scale), both rounded to ``dtype``."""
+    x = normal((B, T, d_model), dtype=dtype, seed=seed, layer=layer, stream="x")
+    g = _gen(seed, layer, "w")
+    w = torch.randn((rows, d_model), generator=g, dtype=torch.float32) / float(d_model) ** 0.5
+    return x, w.to(dtype)

@@ -223,6 +223,39 @@ SFA_API sfa_status sfa_forward_noalloc(const sfa_params *p, const void *Q, const
                                        const void *V, const float *rope_table, void *O,
                                        float *lse, unsigned int *status, cudaStream_t stream);
 
+/* ---- fused front end: QKV projection with RoPE ---------------------- */
+
+/* The step before the attention of a layer (section 3 "Model and training":
+ * d_model 512, 8 query and 2 key/value heads of dimension 64; section 2
+ * "Attended set": RoPE at the true positions before any key row is
+ * gathered): [Q | K | V] = X . Wqkv^T, then Q and K rotated,
+ *   Qhat[b][i][h][:] = R(i) Q[b][i][h][:],  Khat[b][i][g][:] = R(i) K[b][i][g][:],
+ * R(i) the rotate-half rotation of pairs (m, m + 32) by the angle
+ * i * rope_theta^(-2m/64) (the table of sfa_rope_table).  sfa_forward with
+ * rope_theta = 0 then computes the same attention as sfa_forward on the
+ * unrotated Q, K with rope_theta set.
+ *   p: B, T, Hq = 8, Hkv = 2, D = 64, dtype SFA_BF16 and rope_theta are used
+ *     (rope_theta = 0: no rotation, a plain projection); the other fields are
+ *     validated as for sfa_forward but not used;
+ *   d_model: a multiple of 64, 64 .. 16384;
+ *   X [B][T][d_model] bf16, row-major;
+ *   Wqkv [768][d_model] bf16, row-major (the weight of a linear layer): rows
+ *     64h .. 64h + 63 produce query head h (h < 8), rows 512 + 64g .. key
+ *     head g, rows 640 + 64g .. value head g (g < 2); row r of a block is
+ *     dimension r mod 64;
+ *   rope_table: >= T positions (device, from sfa_rope_table); NULL when
+ *     rope_theta = 0;
+ *   Qhat [B][T][8][64], Khat [B][T][2][64], V [B][T][2][64] bf16 (outputs,
+ *     natural dimension order);
+ *   status: device word or NULL (SFA_DEVSTAT_WAIT_TIMEOUT if a pipeline wait
+ *     gave up; the outputs are then not written).
+ * All device pointers 16-byte aligned.  One launch on the tensor cores
+ * (tcgen05, fp32 accumulation in tensor memory); allocates nothing.
+ * Asynchronous on stream. */
+SFA_API sfa_status sfa_qkv_rope(const sfa_params *p, int d_model, const void *X, const void *Wqkv,
+                                const float *rope_table, void *Qhat, void *Khat, void *V,
+                                unsigned int *status, cudaStream_t stream);
+
 /* ---- decode ------------------------------------------------------------ */
 
 /* One new query per sequence over a key/value cache: the attention of query

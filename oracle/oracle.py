@@ -182,6 +182,28 @@ def rope(x, rope_theta: float = 1e4, inverse: bool = False) -> np.ndarray:
     return y
 
 
+def qkv_rope(x, w, *, Hq: int = 8, Hkv: int = 2, D: int = 64, rope_theta: float = 1e4):
+    """The front end of a layer in fp64: [Q | K | V] = x w^T (section 3,
+    "Model and training": d_model 512, 8 query and 2 key/value heads of
+    dimension 64), then Q and K rotated at their true positions (section 2,
+    "Attended set": RoPE before any key row is gathered).
+
+    x [B, T, d_model]; w [(Hq + 2 Hkv) D, d_model], the rows of query head h
+    first (h D .. h D + D - 1), then the key heads, then the value heads.
+    Returns (qhat [B,T,Hq,D], khat [B,T,Hkv,D], v [B,T,Hkv,D])."""
+    x, w = _f64(x), _f64(w)
+    B, T, dm = x.shape
+    if w.shape != ((Hq + 2 * Hkv) * D, dm):
+        raise ValueError(f"w must be [{(Hq + 2 * Hkv) * D}, {dm}], got {w.shape}")
+    y = x.reshape(B * T, dm) @ w.T
+    q = np.ascontiguousarray(y[:, :Hq * D]).reshape(B, T, Hq, D)
+    k = np.ascontiguousarray(y[:, Hq * D:(Hq + Hkv) * D]).reshape(B, T, Hkv, D)
+    v = np.ascontiguousarray(y[:, (Hq + Hkv) * D:]).reshape(B, T, Hkv, D)
+    if rope_theta > 0:
+        q, k = rope(q, rope_theta), rope(k, rope_theta)
+    return q, k, v
+
+
 # ---------------------------------------------- schedules and base tables --
 
 FIBONACCI_BASE = (1, 2, 3, 5, 8, 13, 21, 34, 55, 89, 144, 233, 377, 610, 987)

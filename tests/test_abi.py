@@ -251,3 +251,23 @@ def test_decode_host_checks(lib):
     none = api.Params(0, 64, W=12, alpha=1.0, rope_theta=0.0)
     assert lib.sfa_decode(none.ref(), null, null, null, null, null, null, None, null,
                           null) == _lib.SFA_OK                        # nothing to do
+
+
+def test_qkv_rope_validation(lib):
+    """Host checks of sfa_qkv_rope (no launch): dtype, d_model, pointers."""
+    fake = ctypes.c_void_p(0x10000)   # never dereferenced: every call below fails validation
+    odd = ctypes.c_void_p(0x10008)
+    tab = ctypes.c_void_p(0x20000)
+    p = api.Params(2, 64, W=0, alpha=1.0)
+    args = lambda dm, x=fake, t=tab: (p.ref(), dm, x, fake, t, fake, fake, fake, None, None)
+    assert lib.sfa_qkv_rope(*args(100)) == _lib.SFA_ERR_INVALID_ARG      # not a multiple of 64
+    assert lib.sfa_qkv_rope(*args(0)) == _lib.SFA_ERR_INVALID_ARG
+    assert lib.sfa_qkv_rope(*args(32768)) == _lib.SFA_ERR_INVALID_ARG
+    assert lib.sfa_qkv_rope(*args(512, x=odd)) == _lib.SFA_ERR_INVALID_ARG   # misaligned X
+    assert lib.sfa_qkv_rope(*args(512, t=None)) == _lib.SFA_ERR_INVALID_ARG  # RoPE without a table
+    p32 = api.Params(2, 64, W=0, alpha=1.0, dtype=__import__("torch").float32)
+    assert lib.sfa_qkv_rope(p32.ref(), 512, fake, fake, tab, fake, fake, fake, None, None) == \
+        _lib.SFA_ERR_UNSUPPORTED
+    empty = api.Params(0, 64, W=0, alpha=1.0)
+    assert lib.sfa_qkv_rope(empty.ref(), 512, None, None, None, None, None, None, None, None) == \
+        _lib.SFA_OK

@@ -478,3 +478,49 @@ def test_round_offsets_backward_matches_autograd_and_dalpha_is_zero():
     assert np.max(np.abs(dq - oracle.rope(qh.grad.numpy(), inverse=True))) < 1e-11
     assert np.max(np.abs(dk - oracle.rope(kh.grad.numpy(), inverse=True))) < 1e-11
     assert np.max(np.abs(dv - v.grad.numpy())) < 1e-11
+
+
+# ------------------------------------------------- the QKV front end ----
+
+
+def test_qkv_front_end_brute_force_and_complex_rotation():
+    """oracle.qkv_rope against explicit loops for the projection and complex
+    multiplication z e^{i p w_m} (z = x_m + i x_{m+32}, w_m = 1e4^(-2m/64)) for
+    the rotation, on a tiny case."""
+    rng = np.random.default_rng(5)
+    B, T, dm = 1, 3, 64
+    x = rng.standard_normal((B, T, dm))
+    w = rng.standard_normal((768, dm)) / 8.0
+    q, k, v = oracle.qkv_rope(x, w, rope_theta=1e4)
+    y = np.zeros((T, 768))
+    for t in range(T):
+        for r in range(768):
+            acc = 0.0
+            for c in range(dm):
+                acc += x[0, t, c] * w[r, c]
+            y[t, r] = acc
+    freq = 10000.0 ** (-2.0 * np.arange(32) / 64)
+    for t in range(T):
+        rot = np.exp(1j * t * freq)
+        for blk, got in ((range(8), q), (range(8, 10), k)):
+            for n, h in enumerate(blk):
+                z = (y[t, 64 * h:64 * h + 32] + 1j * y[t, 64 * h + 32:64 * h + 64]) * rot
+                assert np.max(np.abs(got[0, t, n, :32] - z.real)) < 1e-12
+                assert np.max(np.abs(got[0, t, n, 32:] - z.imag)) < 1e-12
+        for g in range(2):
+            assert np.max(np.abs(v[0, t, g] - y[t, 640 + 64 * g:704 + 64 * g])) < 1e-12
+    q0, k0, v0 = oracle.qkv_rope(x, w, rope_theta=0.0)
+    assert np.max(np.abs(q0[0, :, 3] - y[:, 192:256])) < 1e-12
+    assert np.array_equal(v0, v)
+
+
+def test_front_end_then_unrotated_attention_equals_attention_with_rope():
+    """Rotating in the front end and attending with the rotation off gives the
+    attention with RoPE inside (the rotation is applied once, before the
+    gather, at true positions)."""
+    x, w = inputs.hidden_and_weight(1, 40, 128, dtype=torch.float32, layer=3)
+    q, k, v = oracle.qkv_rope(f64(x), f64(w), rope_theta=0.0)
+    qh, kh, v2 = oracle.qkv_rope(f64(x), f64(w), rope_theta=1e4)
+    o1, l1 = oracle.forward(q, k, v, W=4, rungs=oracle.FIBONACCI_BASE, alpha=0.83, rope_theta=1e4)
+    o2, l2 = oracle.forward(qh, kh, v2, W=4, rungs=oracle.FIBONACCI_BASE, alpha=0.83, rope_theta=0.0)
+    assert np.max(np.abs(o1 - o2)) < 1e-12 and np.max(np.abs(l1 - l2)) < 1e-12
