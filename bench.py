@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="model-shape",
                     choices=["model-shape", "extrapolation", "pow2", "train-step", "long-forward",
-                             "decode"])
+                             "decode", "front-end"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     return ap.parse_args()
@@ -505,6 +505,101 @@ def run_decode(args, rank, world, local):
         print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------- front-end arm --
+
+def measured_tflops(kind="bf16_tflops_sustained"):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)[kind]), f"measured ({kind})"
+    except Exception:
+        return 1700.0, "fallback"
+
+
+def run_front_end(args, rank, world, local):
+    """A layer with its fused front end: one step = for each of the 16
+    model-shape layers (B=32, T=1024, W=12, linear stagger), sfa_qkv_rope on
+    that layer's hidden states X [32, 1024, 512] with its weight Wqkv [768, 512]
+    (RoPE in the epilogue), then sfa_forward on the rotated tensors with the
+    rotation off.  Every layer has its own seeded X and Wqkv resident in HBM
+    (537 MB of X per step, larger than L2).  ``value`` counts query tokens;
+    the roofline is the front-end kernel's (a dense contraction: tensor-bound,
+    2 x 768 x 512 flops per token) against the sustained cuBLAS bf16 rate."""
+    import torch
+    from fibonacci_spaced_sparse_gb300 import api, inputs
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = workload_of("model-shape")
+    alphas, _ = wl.alphas()
+    L, B, T, dm = wl.layers, wl.B, wl.T, 512
+    xw = [inputs.hidden_and_weight(B, T, dm, seed=42 + 1000 * rank, layer=l) for l in range(L)]
+    xs = [x.to(dev) for x, _ in xw]
+    wts = [w.to(dev) for _, w in xw]
+    bf = torch.bfloat16
+    bufs = [(torch.empty((B, T, 8, 64), dtype=bf, device=dev),
+             torch.empty((B, T, 2, 64), dtype=bf, device=dev),
+             torch.empty((B, T, 2, 64), dtype=bf, device=dev)) for _ in range(2)]
+    outs = [torch.empty((B, T, 8, 64), dtype=bf, device=dev) for _ in range(L)]
+    lses = [torch.empty((B, T, 8), dtype=torch.float32, device=dev) for _ in range(L)]
+    api.rope_table(T, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        for l in range(L):
+            if ev is not None:
+                ev[3 * l].record(stream)
+            qh, kh, v = api.sfa_qkv_rope(xs[l], wts[l], out=bufs[l & 1])
+            if ev is not None:
+                ev[3 * l + 1].record(stream)
+            api.sfa_forward(qh, kh, v, alpha=alphas[l], W=wl.window(l), rope_theta=0.0,
+                            out=outs[l], lse=lses[l])
+            if ev is not None:
+                ev[3 * l + 2].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    steps = max(1, args.steps)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * L)] for _ in range(steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = api.launch_count()
+    with ClockSampler(local) as clk:
+        torch.cuda.synchronize(dev)
+        start.record(stream)
+        for s_ in range(steps):
+            step(ev[s_])
+        stop.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = api.launch_count() - n0
+    ms = start.elapsed_time(stop)
+    qkv_us = statistics.mean(e[3 * l].elapsed_time(e[3 * l + 1]) for e in ev for l in range(L)) * 1e3
+    att_us = statistics.mean(e[3 * l + 1].elapsed_time(e[3 * l + 2]) for e in ev for l in range(L)) * 1e3
+    flops = 2.0 * 768 * dm * B * T
+    tpeak, tkind = measured_tflops()
+    hpeak, hkind = measured_peak()
+    achieved = flops / (qkv_us * 1e-6) / 1e12
+    io_bytes = (dm * 2 + 768 * 2) * B * T  # read X, write Qhat, Khat, V (bf16)
+    line = {
+        "metric": "layer with fused QKV+RoPE front end, query-tokens/s (T=1024,W=12,bf16)",
+        "value": B * T * L * steps / (ms / 1e3), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "model-shape layers with the QKV+RoPE front end", "B": B, "T": T,
+                   "W": list(wl.W), "layers": L, "d_model": dm, "schedule": wl.schedule,
+                   "l2": "537 MB of X per step, larger than L2, no flush"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": tpeak, "unit": "TFLOP/s",
+                     "frac": achieved / tpeak, "traffic": None, "kernel": "qkv_rope_kernel",
+                     "flops_per_launch": flops, "avg_launch_us": qkv_us, "peak_kind": tkind,
+                     "hbm": {"ideal_bytes_per_launch": io_bytes,
+                             "achieved_gbs": io_bytes / (qkv_us * 1e-6) / 1e9, "peak": hpeak,
+                             "peak_kind": hkind}},
+        "attention_rope_off_us": att_us,
+        "e2e": None, "gpu_launches": launches, "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 # --------------------------------------------------------- reference arm --
 
 def run_reference(args, rank, world):
@@ -562,6 +657,9 @@ def main():
     build.build()
     if args.workload == "decode":
         run_decode(args, rank, world, local)
+        return
+    if args.workload == "front-end":
+        run_front_end(args, rank, world, local)
         return
     run_ours(args, rank, world, local)
 
