@@ -61,6 +61,59 @@ def dist_env():
     return rank, world, local
 
 
+# ---------------------------------------------------------------- replicas --
+#
+# With N > 1 (one process per GPU under torchrun) every rank runs its own
+# independent batch of sequences -- the path shards over sequences with no
+# exchange -- and the job's time is the slowest rank's.
+
+def replica_seed(rank: int) -> int:
+    """Seed of a rank's inputs: each rank draws its own batch."""
+    return 42 + 1000 * int(rank)
+
+
+def init_dist(world: int, dev=None, backend: str = "nccl") -> bool:
+    """Joins the process group when world > 1 (127.0.0.1 rendezvous from the
+    launcher's environment); returns whether there is one."""
+    if world <= 1:
+        return False
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        if backend == "nccl":
+            dist.init_process_group(backend, device_id=dev)
+        else:
+            dist.init_process_group(backend)
+    return True
+
+
+def max_over_ranks(ms: float, device=None) -> float:
+    """The slowest rank's time, returned on every rank (as is without a
+    process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    """All ranks meet (and the device is idle) before and after a timed region."""
+    import torch
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+    if device is not None and torch.cuda.is_available():
+        torch.cuda.synchronize(device)
+
+
+def aggregate_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest
+    rank's time in milliseconds."""
+    return float(units_per_rank) * int(world) / (float(ms) / 1e3)
+
+
 def workload_of(name):
     from fibonacci_spaced_sparse_gb300 import workloads as w
     return {"model-shape": w.MODEL_SHAPE, "extrapolation": w.EXTRAPOLATION, "pow2": w.POW2,
@@ -206,7 +259,7 @@ def run_ours(args, rank, world, local):
     L = wl.layers
     bf = torch.bfloat16
     # every rank holds its own batch (weak scaling: replicas over independent sequences)
-    host = [inputs.qkv(wl.B, wl.T, dtype=bf, seed=42 + 1000 * rank, layer=l, with_dO=wl.backward)
+    host = [inputs.qkv(wl.B, wl.T, dtype=bf, seed=replica_seed(rank), layer=l, with_dO=wl.backward)
             for l in range(L)]
     dv = [{k: v.to(dev) for k, v in h.items()} for h in host]
     outs = [torch.empty_like(d["q"]) for d in dv]
@@ -240,20 +293,11 @@ def run_ours(args, rank, world, local):
                 if events is not None:
                     events[3 + 2 * l].record(stream)
 
-    use_dist = world > 1
-    if use_dist:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if use_dist:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize(dev)
+    use_dist = init_dist(world, dev)
 
     for _ in range(max(3, args.warmup)):
         step()
-    barrier()
+    barrier(dev)
 
     # device-timed region: K steps, per-launch events on the launching stream
     nev = 2 + (2 * L if wl.backward else 0)
@@ -261,24 +305,19 @@ def run_ours(args, rank, world, local):
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n0 = api.launch_count()
     with ClockSampler(local) as clk:
-        barrier()
+        barrier(dev)
         start.record(stream)
         for s in range(args.steps):
             step(ev[s])
         stop.record(stream)
-        barrier()
+        barrier(dev)
     launches = api.launch_count() - n0
     elapsed_ms = start.elapsed_time(stop)
     # per-layer average of the forward (the multi-layer call's time / L)
     fwd_ms = [st[0].elapsed_time(st[1]) / L for st in ev]
     bwd_ms = [st[2 + 2 * l].elapsed_time(st[3 + 2 * l]) for st in ev for l in range(L)] if wl.backward else []
-    if use_dist:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-    tokens = wl.B * wl.T * L * args.steps * world
-    value = tokens / (elapsed_ms / 1e3)
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    value = aggregate_rate(wl.B * wl.T * L * args.steps, world, elapsed_ms)
 
     # roofline of the forward kernel
     peak, peak_kind = measured_peak()
@@ -397,14 +436,9 @@ def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
         step()
     stop.record(stream)
     torch.cuda.synchronize(dev)
-    ms = start.elapsed_time(stop)
-    if use_dist:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = wl.B * wl.T * L * steps * world
-    return {"value": tokens / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    ms = max_over_ranks(start.elapsed_time(stop), dev)
+    return {"value": aggregate_rate(wl.B * wl.T * L * steps, world, ms), "unit": UNIT,
+            "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps}
 
 
@@ -424,8 +458,9 @@ def run_decode(args, rank, world, local):
     wl = workload_of("decode")
     alphas, _ = wl.alphas()
     L, B, Tc, W = wl.layers, wl.B, wl.T, wl.window(0)
+    use_dist = init_dist(world, dev)
     gen = torch.Generator(device=dev)
-    gen.manual_seed(42 + 1000 * rank)
+    gen.manual_seed(replica_seed(rank))
     shape = (B, Tc, 2, 64)
     kc = [torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
     vc = [torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16) for _ in range(L)]
@@ -458,17 +493,18 @@ def run_decode(args, rank, world, local):
 
     for _ in range(max(3, args.warmup)):
         step()
-    torch.cuda.synchronize(dev)
+    barrier(dev)
     steps = max(1, args.steps)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        barrier(dev)
         start.record(stream)
         for _ in range(steps):
             step()
         stop.record(stream)
-        torch.cuda.synchronize(dev)
+        barrier(dev)
     launches = L * steps  # graph replays: the library's counter sees only the capture
-    ms = start.elapsed_time(stop)
+    ms = max_over_ranks(start.elapsed_time(stop), dev)
     # bytes one step must move: every layer's Q and O rows, and the distinct
     # cache rows (key and value, both kv heads) of each sequence's key list
     p_host = pos.cpu().numpy()
@@ -489,7 +525,7 @@ def run_decode(args, rank, world, local):
     achieved = step_bytes / L / per_layer_s / 1e9
     line = {
         "metric": "sparse-attn decode tokens/s (one new token per sequence through 16 layers)",
-        "value": B * steps / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "value": aggregate_rate(B * steps, world, ms), "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "B": B, "cache_rows": Tc, "W": [W], "layers": L,
@@ -503,6 +539,9 @@ def run_decode(args, rank, world, local):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if use_dist:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 # --------------------------------------------------------- front-end arm --
@@ -532,7 +571,8 @@ def run_front_end(args, rank, world, local):
     wl = workload_of("model-shape")
     alphas, _ = wl.alphas()
     L, B, T, dm = wl.layers, wl.B, wl.T, 512
-    xw = [inputs.hidden_and_weight(B, T, dm, seed=42 + 1000 * rank, layer=l) for l in range(L)]
+    use_dist = init_dist(world, dev)
+    xw = [inputs.hidden_and_weight(B, T, dm, seed=replica_seed(rank), layer=l) for l in range(L)]
     xs = [x.to(dev) for x, _ in xw]
     wts = [w.to(dev) for _, w in xw]
     bf = torch.bfloat16
@@ -558,20 +598,20 @@ def run_front_end(args, rank, world, local):
 
     for _ in range(max(3, args.warmup)):
         step()
-    torch.cuda.synchronize(dev)
+    barrier(dev)
     steps = max(1, args.steps)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * L)] for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n0 = api.launch_count()
     with ClockSampler(local) as clk:
-        torch.cuda.synchronize(dev)
+        barrier(dev)
         start.record(stream)
         for s_ in range(steps):
             step(ev[s_])
         stop.record(stream)
-        torch.cuda.synchronize(dev)
+        barrier(dev)
     launches = api.launch_count() - n0
-    ms = start.elapsed_time(stop)
+    ms = max_over_ranks(start.elapsed_time(stop), dev)
     qkv_us = statistics.mean(e[3 * l].elapsed_time(e[3 * l + 1]) for e in ev for l in range(L)) * 1e3
     att_us = statistics.mean(e[3 * l + 1].elapsed_time(e[3 * l + 2]) for e in ev for l in range(L)) * 1e3
     flops = 2.0 * 768 * dm * B * T
@@ -581,7 +621,8 @@ def run_front_end(args, rank, world, local):
     io_bytes = (dm * 2 + 768 * 2) * B * T  # read X, write Qhat, Khat, V (bf16)
     line = {
         "metric": "layer with fused QKV+RoPE front end, query-tokens/s (T=1024,W=12,bf16)",
-        "value": B * T * L * steps / (ms / 1e3), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "value": aggregate_rate(B * T * L * steps, world, ms), "unit": UNIT, "n_gpus": world,
+        "steps": steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms / steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": "model-shape layers with the QKV+RoPE front end", "B": B, "T": T,
@@ -598,6 +639,9 @@ def run_front_end(args, rank, world, local):
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
+    if use_dist:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 # --------------------------------------------------------- reference arm --
