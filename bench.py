@@ -187,11 +187,17 @@ class ClockSampler:
 
 # --------------------------------------------------------- traffic record --
 
+# The sources that decide what the forward attention kernel does: its own
+# file, the ring and PTX helpers it includes, and the host code that plans
+# rungs and launches it.
+FORWARD_SOURCES = ("sfa_fwd_mma.cu", "sfa_ring.cuh", "sfa_mma.cuh", "sfa_internal.cuh", "sfa_api.cu")
+
+
 def kernel_source_digest():
     from fibonacci_spaced_sparse_gb300 import build
     h = hashlib.sha256()
-    for p in sorted(build.sources()):
-        with open(p, "rb") as fh:
+    for name in FORWARD_SOURCES:
+        with open(os.path.join(build.CSRC, name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -532,7 +538,7 @@ def run_decode(args, rank, world, local):
                    "schedule": wl.schedule, "base": wl.base,
                    "l2": "caches of 8.6 GB, rows read cold each step"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "decode_kernel",
+                     "frac": achieved / peak, "traffic": None, "kernel": "decode_fast_kernel",
                      "ideal_bytes_per_launch": step_bytes / L, "avg_launch_us": per_layer_s * 1e6,
                      "peak_kind": peak_kind},
         "gpu_launches": launches, "clocks": clk.summary(),

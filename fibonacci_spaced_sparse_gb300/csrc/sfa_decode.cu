@@ -188,13 +188,209 @@ decode_kernel(const LayerArgs a, int Tc, const T* __restrict__ q, const T* __res
     }
 }
 
+// ---------------------------------------------------------- bf16, W <= 16
+//
+// The key list of a query has at most W + 1 + K <= 32 entries here, so one
+// CTA of four warps holds all of them at once: lane = (entry e of the warp's
+// eight, 16-dimension chunk c).  Chunk c is the RoPE pairs m = 8c .. 8c + 7,
+// i.e. dimensions 8c .. 8c + 7 and their partners 32 + 8c .. 32 + 8c + 7, two
+// 16-byte pieces of a row, and the (cos, sin) of those pairs are 64
+// contiguous bytes of the table row, so every load of a cache row is a
+// 16-byte load and all of an entry's rows are in flight together.  A score is
+// the sum of four lanes' partial dot products (two shuffles); the maximum and
+// the sum over the entries go through the warp and a few shared words; the
+// value products of the 32 entries are summed through shared memory (entry
+// stride padded so that the 16-byte writes of a warp hit distinct banks).
+constexpr int kFastEntries = 32;
+constexpr int kFastThreads = 128;
+constexpr int kRedStride = 4 * kD + 4;  // floats per entry in the value-product buffer
+
+__device__ __forceinline__ float2 bf2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+// Rotated (x, y) halves of the 8 pairs of chunk c of a cache row, fp32.
+__device__ __forceinline__ void load_row(const __nv_bfloat16* __restrict__ base, const float2* __restrict__ rope,
+                                         int pos, int c, float (&x)[8], float (&y)[8], float (&v)[16],
+                                         const __nv_bfloat16* __restrict__ vbase) {
+    const uint4 kx = __ldg(reinterpret_cast<const uint4*>(base) + c);
+    const uint4 ky = __ldg(reinterpret_cast<const uint4*>(base) + 4 + c);
+    const uint4 vx = __ldg(reinterpret_cast<const uint4*>(vbase) + c);
+    const uint4 vy = __ldg(reinterpret_cast<const uint4*>(vbase) + 4 + c);
+    float4 cs[4];
+    if (rope) {
+        const float4* t = reinterpret_cast<const float4*>(rope + (size_t)pos * kPairs + 8 * c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cs[j] = __ldg(t + j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cs[j] = make_float4(1.f, 0.f, 1.f, 0.f);
+    }
+    const uint32_t kxw[4] = {kx.x, kx.y, kx.z, kx.w}, kyw[4] = {ky.x, ky.y, ky.z, ky.w};
+    const uint32_t vxw[4] = {vx.x, vx.y, vx.z, vx.w}, vyw[4] = {vy.x, vy.y, vy.z, vy.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float2 a = bf2(kxw[j]), b = bf2(kyw[j]);
+        // pairs 2j, 2j + 1 of the chunk: (cos, sin) in cs[j].xy and cs[j].zw
+        x[2 * j] = a.x * cs[j].x - b.x * cs[j].y;
+        y[2 * j] = b.x * cs[j].x + a.x * cs[j].y;
+        x[2 * j + 1] = a.y * cs[j].z - b.y * cs[j].w;
+        y[2 * j + 1] = b.y * cs[j].z + a.y * cs[j].w;
+        const float2 p = bf2(vxw[j]), q = bf2(vyw[j]);
+        v[2 * j] = p.x;
+        v[2 * j + 1] = p.y;
+        v[8 + 2 * j] = q.x;
+        v[8 + 2 * j + 1] = q.y;
+    }
+}
+
+__global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
+    const LayerArgs a, int Tc, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
+    const __nv_bfloat16* __restrict__ vc, const int* __restrict__ pos, const float2* __restrict__ rope,
+    __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* __restrict__ status) {
+    __shared__ __align__(16) float qh[kG][kD];                   // the rotated query, fp32
+    __shared__ __align__(16) float red[kFastEntries * kRedStride];  // p v per entry
+    __shared__ float mw[4][kG], lw[4][kG];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = blockIdx.x % kHkv, b = blockIdx.x / kHkv;
+    const int i = __ldg(pos + b);
+    const size_t qbase = ((size_t)b * kHq + g * kG) * kD;
+    if (i < 0 || i >= Tc) {
+        // a position outside the cache: report it, read nothing, output zeros
+        if (tid == 0 && status) atomicOr(status, SFA_DEVSTAT_BAD_INDEX);
+        o[qbase + 2 * tid] = __float2bfloat16_rn(0.f);
+        o[qbase + 2 * tid + 1] = __float2bfloat16_rn(0.f);
+        if (lse && tid < kG) lse[(size_t)b * kHq + g * kG + tid] = 0.f;
+        return;  // the whole CTA leaves together
+    }
+    // the query: thread (h, m) rotates pair m of head h
+    {
+        const int h = tid >> 5, m = tid & 31;
+        const float x = __bfloat162float(q[qbase + h * kD + m]), y = __bfloat162float(q[qbase + h * kD + kPairs + m]);
+        const float2 cs = rope_cs(rope, i, m);
+        qh[h][m] = x * cs.x - y * cs.y;
+        qh[h][kPairs + m] = y * cs.x + x * cs.y;
+    }
+    // this lane's entry: window distances 0..min(W, i), then the rungs with
+    // ceil(d) <= i (a prefix of the kept list, which is sorted by distance)
+    const int c = lane & 3, e = warp * 8 + (lane >> 2);
+    const int nwin = min(a.W, i) + 1;
+    int nact = 0;
+    for (int r = 0; r < a.nr; ++r) nact += (a.r[r].c <= i) ? 1 : 0;
+    const bool live = e < nwin + nact;
+    int ra = i, rb = -1;
+    float wa = 1.f, wb = 0.f;
+    if (live && e >= nwin) {
+        const Rung R = a.r[e - nwin];
+        ra = i - R.n;
+        rb = R.t > 0.f ? ra - 1 : -1;
+        wa = 1.f - R.t;
+        wb = R.t;
+    } else if (live) {
+        ra = i - e;
+    }
+    float kx[8], ky[8], vv[16];
+    {
+        const size_t off = (((size_t)b * Tc + ra) * kHkv + g) * kD;
+        load_row(kc + off, rope, ra, c, kx, ky, vv, vc + off);
+    }
+    if (rb >= 0) {
+        float bx[8], by[8], bv[16];
+        const size_t off = (((size_t)b * Tc + rb) * kHkv + g) * kD;
+        load_row(kc + off, rope, rb, c, bx, by, bv, vc + off);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            kx[j] = wa * kx[j] + wb * bx[j];
+            ky[j] = wa * ky[j] + wb * by[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) vv[j] = wa * vv[j] + wb * bv[j];
+    }
+    __syncthreads();  // qh
+    const float sl2 = a.scale * kLog2e;
+    float s[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+        const float4* qx = reinterpret_cast<const float4*>(&qh[h][8 * c]);
+        const float4* qy = reinterpret_cast<const float4*>(&qh[h][kPairs + 8 * c]);
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const float4 u = qx[j], w = qy[j];
+            acc += u.x * kx[4 * j] + u.y * kx[4 * j + 1] + u.z * kx[4 * j + 2] + u.w * kx[4 * j + 3];
+            acc += w.x * ky[4 * j] + w.y * ky[4 * j + 1] + w.z * ky[4 * j + 2] + w.w * ky[4 * j + 3];
+        }
+        acc += __shfl_xor_sync(kFull, acc, 1);
+        acc += __shfl_xor_sync(kFull, acc, 2);
+        s[h] = live ? acc * sl2 : -INFINITY;
+    }
+    // the maximum over the key list (entry 0, the query's own row, is always live)
+    float mx[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+        mx[h] = s[h];
+#pragma unroll
+        for (int w = 4; w <= 16; w <<= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], w));
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int h = 0; h < kG; ++h) mw[warp][h] = mx[h];
+    }
+    __syncthreads();
+    float p[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+        const float M = fmaxf(fmaxf(mw[0][h], mw[1][h]), fmaxf(mw[2][h], mw[3][h]));
+        p[h] = live ? exp2f(s[h] - M) : 0.f;
+        float l = p[h];
+#pragma unroll
+        for (int w = 4; w <= 16; w <<= 1) l += __shfl_xor_sync(kFull, l, w);
+        if (lane == 0) lw[warp][h] = l;
+        mx[h] = M;
+    }
+    // p v of this entry, chunk c, into the reduction buffer
+    float* rr = red + e * kRedStride;
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+        float4* dx = reinterpret_cast<float4*>(rr + h * kD + 8 * c);
+        float4* dy = reinterpret_cast<float4*>(rr + h * kD + kPairs + 8 * c);
+        dx[0] = make_float4(p[h] * vv[0], p[h] * vv[1], p[h] * vv[2], p[h] * vv[3]);
+        dx[1] = make_float4(p[h] * vv[4], p[h] * vv[5], p[h] * vv[6], p[h] * vv[7]);
+        dy[0] = make_float4(p[h] * vv[8], p[h] * vv[9], p[h] * vv[10], p[h] * vv[11]);
+        dy[1] = make_float4(p[h] * vv[12], p[h] * vv[13], p[h] * vv[14], p[h] * vv[15]);
+    }
+    __syncthreads();
+    // thread (h, d): outputs d and d + 32 of head h, summed over the entries in order
+    {
+        const int h = tid >> 5, d = tid & 31;
+        float o0 = 0.f, o1 = 0.f;
+#pragma unroll 8
+        for (int en = 0; en < kFastEntries; ++en) {
+            o0 += red[en * kRedStride + h * kD + d];
+            o1 += red[en * kRedStride + h * kD + kPairs + d];
+        }
+        const float L = (lw[0][h] + lw[1][h]) + (lw[2][h] + lw[3][h]);
+        const float inv = 1.f / L;
+        o[qbase + h * kD + d] = __float2bfloat16_rn(o0 * inv);
+        o[qbase + h * kD + kPairs + d] = __float2bfloat16_rn(o1 * inv);
+        if (lse && d == 0) {
+            const float M = fmaxf(fmaxf(mw[0][h], mw[1][h]), fmaxf(mw[2][h], mw[3][h]));
+            lse[(size_t)b * kHq + g * kG + h] = (M + log2f(L)) * kLn2;
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const LayerArgs& a, int Tc, sfa_dtype dt, const void* q, const void* kc,
                           const void* vc, const int* pos, const float2* rope, void* o, float* lse,
                           unsigned* status, cudaStream_t s) {
     const int blocks = a.B * kHkv;
-    if (dt == SFA_F32)
+    if (dt == SFA_BF16 && a.W + 1 + a.nr <= kFastEntries) {
+        decode_fast_kernel<<<blocks, kFastThreads, 0, s>>>(a, Tc, (const __nv_bfloat16*)q, (const __nv_bfloat16*)kc,
+                                                         (const __nv_bfloat16*)vc, pos, rope, (__nv_bfloat16*)o, lse,
+                                                         status);
+    } else if (dt == SFA_F32)
         decode_kernel<float><<<blocks, kSplit * 32, 0, s>>>(a, Tc, (const float*)q, (const float*)kc,
                                                             (const float*)vc, pos, rope, (float*)o, lse,
                                                             status);
