@@ -86,3 +86,10 @@ def test_decode_bad_position_reports_and_zeroes():
     on = np64(o)
     assert np.all(on[1] == 0) and np.all(on[2] == 0)
     assert np.isfinite(on).all() and np.abs(on[0]).max() > 0
+
+
+@pytest.mark.parametrize("alpha,W", [(1.0, 30), (0.7, 24), (1.0, 20), (1.3, 16)])
+def test_decode_long_key_lists(alpha, W):
+    """Key lists longer than 32 entries (W = 24, 30) take the general kernel,
+    shorter ones the one-pass kernel; both against the oracle."""
+    _case(16, 1200, "bf16", alpha, W, seed=7)
