@@ -66,6 +66,7 @@ _SIGS = {
     "sfa_forward_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "sfa_forward_noalloc": ([_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "sfa_decode": ([_PP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
+    "sfa_selftest_wait_timeout": ([_VP, _VP], ctypes.c_int),
     "sfa_qkv_rope": ([_PP, ctypes.c_int, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP], ctypes.c_int),
     "sfa_backward_workspace_size": ([_PP], ctypes.c_size_t),
     "sfa_backward": ([_PP] + [_VP] * 13 + [ctypes.c_size_t, _VP, _VP], ctypes.c_int),

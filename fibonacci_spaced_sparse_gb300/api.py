@@ -253,6 +253,14 @@ def sfa_decode(q, k_cache, v_cache, positions, *, alpha: float, W: int, rungs=FI
     return o, (lse if need_lse else None)
 
 
+def sfa_selftest_wait_timeout(status, stream=None):
+    """Runs the failure-path self-test (sfa_selftest_wait_timeout in
+    include/sfa.h) on status's device: a bounded wait that nothing satisfies
+    gives up and sets SFA_DEVSTAT_WAIT_TIMEOUT in the int32 word ``status``."""
+    st = _lib.load().sfa_selftest_wait_timeout(_vp(status), _stream(status.device, stream))
+    _lib.check(st, "sfa_selftest_wait_timeout")
+
+
 def sfa_qkv_rope(x, w_qkv, *, rope_theta: float = 1e4, out=None, status=None, stream=None):
     """The fused front end (sfa_qkv_rope in include/sfa.h): x [B, T, d_model]
     and w_qkv [768, d_model] bf16 on the device; returns (qhat [B, T, 8, 64],

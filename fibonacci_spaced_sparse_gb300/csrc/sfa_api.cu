@@ -380,6 +380,11 @@ SFA_API sfa_status sfa_qkv_rope(const sfa_params* p, int d_model, const void* X,
                                          V, status, stream));
 }
 
+SFA_API sfa_status sfa_selftest_wait_timeout(unsigned int* status, cudaStream_t stream) {
+    if (!status || (reinterpret_cast<uintptr_t>(status) & 3u)) return SFA_ERR_INVALID_ARG;
+    return launched(sfa::launch_wait_selftest(status, stream));
+}
+
 SFA_API size_t sfa_backward_workspace_size(const sfa_params* p) {
     if (validate(p) != SFA_OK) return 0;
     LayerArgs a;

@@ -72,6 +72,8 @@ cudaError_t launch_decode(const LayerArgs& a, int Tc, sfa_dtype dt, const void* 
 cudaError_t launch_qkv_rope(int M, int T, int dm, const void* x, const void* w, const float2* rope, void* q,
                             void* k, void* v, unsigned* status, cudaStream_t s);
 
+cudaError_t launch_wait_selftest(unsigned* status, cudaStream_t s);
+
 size_t bwd_simple_workspace(const LayerArgs& a);
 cudaError_t launch_bwd_simple(const LayerArgs& a, sfa_dtype dt, const void* q, const void* k,
                               const void* v, const void* o, const void* dO, const float* lse,

@@ -256,6 +256,19 @@ SFA_API sfa_status sfa_qkv_rope(const sfa_params *p, int d_model, const void *X,
                                 const float *rope_table, void *Qhat, void *Khat, void *V,
                                 unsigned int *status, cudaStream_t stream);
 
+/* ---- failure-path self-test ------------------------------------------- */
+
+/* Exercises the failure path that the pipelined kernels share: every wait on
+ * an mbarrier gives up after a fixed limit (0.25 s), sets the CTA's abort
+ * flag so the other warps leave their waits, and sets
+ * SFA_DEVSTAT_WAIT_TIMEOUT in the status word; the kernel then returns and
+ * the context stays usable.  One CTA waits, with those same wait routines, on
+ * a barrier that nothing arrives on.  Touches no data.
+ *   status: device word (required, 4-byte aligned); SFA_DEVSTAT_WAIT_TIMEOUT
+ *     is set in it when the call has run (after about 0.25 s).
+ * One launch; asynchronous on stream. */
+SFA_API sfa_status sfa_selftest_wait_timeout(unsigned int *status, cudaStream_t stream);
+
 /* ---- decode ------------------------------------------------------------ */
 
 /* One new query per sequence over a key/value cache: the attention of query
