@@ -479,7 +479,8 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
 #pragma unroll
     for (int w = 4; w <= 16; w <<= 1)
         l = __fadd2_rn(l, f2(__shfl_xor_sync(kFull, l.x, w), __shfl_xor_sync(kFull, l.y, w)));
-    const float2 inv = f2(1.f / l.x, 1.f / l.y);
+    // l >= 1: the entry at the running max contributes exactly 1
+    const float2 inv = f2(fast_rcp(l.x), fast_rcp(l.y));
     uint32_t r[4][2];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -499,13 +500,12 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
         tma_store_4d(&P.omap, obuf, 0, x.g * kG, x.i0 + u, x.b);
         bulk_commit();
     }
-    if (P.lse && g8 == 0) {
+    if (P.lse) {
+        // lanes g8 = 0 hold the sums of query u + tig / 2, heads 2 (tig & 1) + {0, 1}
         const int iq2 = x.i0 + u + (tig >> 1);
-        if (iq2 < P.a.T) {
-            const float2 v = make_float2((__log2f(l.x) - U.nm.x) * kLn2, (__log2f(l.y) - U.nm.y) * kLn2);
-            *reinterpret_cast<float2*>(P.lse + ((size_t)x.b * P.a.T + iq2) * kHq + x.g * kG +
-                                       2 * (tig & 1)) = v;
-        }
+        const float2 v = make_float2((__log2f(l.x) - U.nm.x) * kLn2, (__log2f(l.y) - U.nm.y) * kLn2);
+        float* dst = P.lse + ((size_t)x.b * P.a.T + iq2) * kHq + x.g * kG + 2 * (tig & 1);
+        if (g8 == 0 && iq2 < P.a.T) *reinterpret_cast<float2*>(dst) = v;
     }
 }
 

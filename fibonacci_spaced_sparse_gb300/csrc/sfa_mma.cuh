@@ -187,6 +187,15 @@ __device__ __forceinline__ float2 unpack_bf16(uint32_t x) {
     return __bfloat1622float2(h);
 }
 
+// 1 / x by the hardware approximation (relative error below 2^-22 for the
+// normal positive x it is used on -- row sums of at least 1 -- far below the
+// bf16 rounding that follows).
+__device__ __forceinline__ float fast_rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
