@@ -72,3 +72,44 @@ def api_ws_fwd(B, T, L):
     p = api.Params(B, T, W=12, alpha=1.0)
     win = (ctypes.c_int * L)(*([12] * L))
     return max(1, int(_lib.load().sfa_forward_layers_workspace_size(p.ref(), L, win)))
+
+
+def test_front_end_and_attention_graph_replay_matches_eager():
+    """sfa_qkv_rope then sfa_forward(rope_theta = 0) for two layers, captured
+    in one graph: the replay reproduces the eager outputs bit for bit."""
+    from fibonacci_spaced_sparse_gb300 import inputs
+    B, T, dm, L = 2, 384, 512, 2
+    xw = [inputs.hidden_and_weight(B, T, dm, layer=30 + l) for l in range(L)]
+    xs = [x.cuda() for x, _ in xw]
+    ws = [w.cuda() for _, w in xw]
+    bf = torch.bfloat16
+    mids = [(torch.empty((B, T, 8, 64), dtype=bf, device="cuda"),
+             torch.empty((B, T, 2, 64), dtype=bf, device="cuda"),
+             torch.empty((B, T, 2, 64), dtype=bf, device="cuda")) for _ in range(L)]
+    outs = [torch.empty((B, T, 8, 64), dtype=bf, device="cuda") for _ in range(L)]
+    lses = [torch.empty((B, T, 8), dtype=torch.float32, device="cuda") for _ in range(L)]
+
+    def step(stream):
+        for l in range(L):
+            qh, kh, v = api.sfa_qkv_rope(xs[l], ws[l], out=mids[l], stream=stream)
+            api.sfa_forward(qh, kh, v, alpha=0.7 + 0.4 * l, W=12, rope_theta=0.0, out=outs[l],
+                            lse=lses[l], stream=stream)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    eager = [(o.clone(), s.clone(), m[0].clone()) for o, s, m in zip(outs, lses, mids)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step(side)
+    for o, m in zip(outs, mids):
+        o.zero_()
+        m[0].zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert torch.equal(outs[l], eager[l][0]) and torch.equal(lses[l], eager[l][1])
+        assert torch.equal(mids[l][0], eager[l][2])
