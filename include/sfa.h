@@ -32,9 +32,12 @@
  *
  * Ownership.  The caller allocates every buffer (outputs, workspace, RoPE
  * table, status word).  The library allocates no device or host memory and
- * keeps no state between calls; the rung table is copied into the kernel
- * arguments.  Every call is asynchronous on the given stream and returns
- * before the GPU finishes.
+ * carries no data from one call to the next; the rung table is copied into
+ * the kernel arguments.  What it keeps is per device and read-only after the
+ * first call there: the SM count, kernel attributes already set, resident
+ * CTAs per SM of its persistent kernels, and sfa_forward_noalloc's fixed
+ * scratch array (part of the library image).  Every call is asynchronous on
+ * the given stream and returns before the GPU finishes.
  *
  * Errors.  Invalid arguments return SFA_ERR_INVALID_ARG and shapes outside the
  * supported set return SFA_ERR_UNSUPPORTED, both before anything is launched.
