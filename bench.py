@@ -38,6 +38,7 @@ UNIT = "query-tokens/s"
 IDEAL_BYTES_PER_TOKEN = 2 * (8 * 64 + 2 * 64 + 2 * 64 + 8 * 64)  # bf16 Q, K, V read + O write
 FALLBACK_HBM_GBS = 6800.0
 E2E_MAX_STEPS = 20
+REFERENCE_BUDGET_S = 90.0  # oracle time of a whole --impl reference run
 
 
 def parse():
@@ -653,8 +654,11 @@ def run_front_end(args, rank, world, local):
 # --------------------------------------------------------- reference arm --
 
 def run_reference(args, rank, world):
-    """The CPU oracle as the reference arm: each step is one whole layer of the
-    workload (B x T query tokens) on all host cores."""
+    """The CPU oracle as the reference arm, on the host cores: each step is a
+    bounded sample of the workload -- a slice of whole sequences of one layer
+    (layers 0..3 in turn) -- sized from a one-sequence calibration so that the
+    warm-up and timed steps together take about REFERENCE_BUDGET_S seconds of
+    oracle time, whatever --steps is."""
     if rank != 0:
         return
     import torch
@@ -664,34 +668,44 @@ def run_reference(args, rank, world):
     wl = workload_of(args.workload)
     alphas, _ = wl.alphas()
     cores = oracle.default_threads()
+    nl = min(wl.layers, 4)
     data = []
-    for l in range(min(wl.layers, args.steps + max(3, args.warmup))):
+    for l in range(nl):
         x = inputs.qkv(wl.B, wl.T, dtype=torch.bfloat16, layer=l)
         data.append({k: v.to(torch.float64).numpy() for k, v in x.items()})
 
-    def step(i):
-        l = i % len(data)
+    def run(l, b0, n):
         f = data[l]
-        oracle.forward(f["q"], f["k"], f["v"], W=wl.window(l), rungs=wl.rungs(), alpha=alphas[l],
-                       nthreads=cores)
+        oracle.forward(f["q"][b0:b0 + n], f["k"][b0:b0 + n], f["v"][b0:b0 + n], W=wl.window(l),
+                       rungs=wl.rungs(), alpha=alphas[l], nthreads=cores)
 
-    for i in range(max(3, args.warmup)):
+    t0 = time.perf_counter()
+    run(0, 0, 1)
+    t_seq = time.perf_counter() - t0
+    warm, steps = max(3, args.warmup), max(1, args.steps)
+    n_seq = int(max(1, min(wl.B, REFERENCE_BUDGET_S / ((warm + steps) * max(t_seq, 1e-6)))))
+
+    def step(i):
+        run(i % nl, (i * n_seq) % (wl.B - n_seq + 1), n_seq)
+
+    for i in range(warm):
         step(i)
     t0 = time.perf_counter()
-    for i in range(args.steps):
-        step(i)
+    for i in range(steps):
+        step(warm + i)
     dt = time.perf_counter() - t0
-    tokens = wl.B * wl.T * args.steps
-    value = tokens / dt
+    value = n_seq * wl.T * steps / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": dt / args.steps * 1e3,
+        "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "W": list(wl.W),
                    "layers": wl.layers, "schedule": wl.schedule, "base": wl.base},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"one whole layer ({wl.B}x{wl.T} query tokens) per step"},
+                         "sample": f"{n_seq} of {wl.B} sequences ({n_seq * wl.T} query tokens) of one "
+                                   f"layer per step, layers 0..{nl - 1} in turn, sized for about "
+                                   f"{REFERENCE_BUDGET_S:.0f} s over {warm + steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
