@@ -125,10 +125,6 @@ __device__ __forceinline__ void stsm_x4_t(uint32_t addr, uint32_t r0, uint32_t r
                  : "memory");
 }
 
-__device__ __forceinline__ void st_zero16(uint32_t dst) {
-    asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(dst), "r"(0u) : "memory");
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -201,8 +197,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-
-__device__ __forceinline__ float shfl(float x, int src) { return __shfl_sync(kFull, x, src); }
 
 }  // namespace mma
 }  // namespace sfa

@@ -288,8 +288,6 @@ __device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
     return v;
 }
 
-__device__ __forceinline__ uint4 ldg_u4(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
-
 __device__ __forceinline__ uint32_t u4_get(const uint4& v, int w) {
     return w == 0 ? v.x : w == 1 ? v.y : w == 2 ? v.z : v.w;
 }
