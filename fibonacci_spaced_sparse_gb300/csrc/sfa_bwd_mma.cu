@@ -23,9 +23,12 @@
 //       dQhat^T += Khat_rows^T . dS^T        (registers, one tile at a time)
 //       dKhat_rows = dS . Qhat, dV_rows = P . dO   (m16n8k8 / m16n8k16)
 //     The interpolation weights split ds and p onto rows a and b inside the
-//     thread, exactly as in the forward.  Rows that several M rows of a warp
-//     share (row a of query i is row b of query i + 1) are summed in registers
-//     and the sums go to the fp32 accumulators with red.global.add.v2.  dQ is
+//     thread, exactly as in the forward.  A window M tile's 16 rows (already
+//     summed over the warp's four queries by the MMA) are staged in shared
+//     memory and added to the fp32 accumulators by four TMA tensor reductions
+//     (cp.reduce.async.bulk.tensor .add); rung rows that several M rows of a
+//     warp share (row a of query i is row b of query i + 1) are summed in
+//     registers and go to the accumulators with red.global.add.v2.  dQ is
 //     rotated back (R(i)^T) and stored through shared memory by TMA; dL/dt is
 //     summed per warp in shared memory and per CTA into the workspace.
 //  3. bwd_finish_kernel: dK = R(j)^T dKhat and dV to the caller's dtype, and
@@ -60,6 +63,7 @@ struct BwdParams {
     CUtensorMap kmap_r[RPG];
     CUtensorMap vmap_r[RPG];
     CUtensorMap dqmap;         // dQ [B][T][8][64], box of 2 queries x 4 heads
+    CUtensorMap dkred, dvred;  // fp32 accumulators [B][T][2][64], box 32 dims x 16 rows, 128-byte swizzle
     LayerArgs a;
     const __nv_bfloat16* q;
     const __nv_bfloat16* o;
@@ -146,6 +150,18 @@ __device__ __forceinline__ void red_v2(float* p, float a, float b, bool ok) {
         "{\n .reg .pred q;\n setp.ne.b32 q, %3, 0;\n @q red.global.add.v2.f32 [%0], {%1, %2};\n}\n" ::"l"(p),
         "f"(a), "f"(b), "r"((int)ok)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_reduce_add_4d(const void* tmap, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+            tmap),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+__device__ __forceinline__ void sts64(uint32_t a, float x, float y) {
+    asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(x), "f"(y) : "memory");
 }
 
 // Address of acc[b][row][g][2 tig] (row_base = b T Hkv + g), and whether the
@@ -240,7 +256,7 @@ __device__ __forceinline__ void start_bunit(const BwdParams& P, const Smem& S, c
 // window block, positions i0 + u0 - W + R).
 template <bool kFirst>
 __device__ __forceinline__ void bwd_window_tile(const BwdParams& P, uint32_t slot, const Tile& x, int u0, int wt,
-                                                const BLane& L, BUnit* U) {
+                                                const BLane& L, BUnit* U, uint32_t stg) {
     const int lane = threadIdx.x & 31;
     const int i0 = x.i0;
     uint32_t kro = L.wk, tro = L.wt;
@@ -309,7 +325,42 @@ __device__ __forceinline__ void bwd_window_tile(const BwdParams& P, uint32_t slo
     // dKhat_rows = dS . Qhat and dV_rows = P . dO over both pairs (k = 16
     // columns), this thread's rows g8 and g8 + 8, dimensions 8 c + 2 tig + {0, 1}
     const int tig = lane & 3;
-    const int r0 = i0 + u0 - P.a.W + 16 * wt + L.g8;
+    const int rstart = i0 + u0 - P.a.W + 16 * wt;
+    if (rstart >= 0) {
+        // stage the 16 rows (dK, dV; two halves of 32 dimensions each, 128-byte
+        // swizzle) and add them with four tensor reductions; rows past T are
+        // clipped by the map, rows outside the quad's window carry zeros.  A
+        // reduction may not start before row 0, so tiles at the sequence
+        // start take the per-thread path below.
+        if (lane == 0) bulk_wait_read();
+        __syncwarp();
+        const int r0s = L.g8, r1s = L.g8 + 8;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            float dk[4], dv[4];
+            mma16816_z(dk, ad[0][0], ad[0][1], ad[1][0], ad[1][1], U[0].qm[c], U[1].qm[c]);
+            mma16816_z(dv, ap[0][0], ap[0][1], ap[1][0], ap[1][1], U[0].dm[c], U[1].dm[c]);
+            const int half = c >> 2, ch = 2 * (c & 3) + (tig >> 1);
+            const uint32_t w = (uint32_t)((2 * tig) & 3) * 4u;
+            const uint32_t a0 = stg + (uint32_t)((half * 16 + r0s) * 128 + (((ch ^ r0s) & 7) << 4)) + w;
+            const uint32_t a1 = stg + (uint32_t)((half * 16 + r1s) * 128 + (((ch ^ r1s) & 7) << 4)) + w;
+            sts64(a0, dk[0], dk[1]);
+            sts64(a1, dk[2], dk[3]);
+            sts64(a0 + 4096u, dv[0], dv[1]);
+            sts64(a1 + 4096u, dv[2], dv[3]);
+        }
+        fence_proxy_async();
+        __syncwarp();
+        if (lane == 0) {
+            tma_reduce_add_4d(&P.dkred, stg, 0, x.g, rstart, x.b);
+            tma_reduce_add_4d(&P.dkred, stg + 2048u, 32, x.g, rstart, x.b);
+            tma_reduce_add_4d(&P.dvred, stg + 4096u, 0, x.g, rstart, x.b);
+            tma_reduce_add_4d(&P.dvred, stg + 6144u, 32, x.g, rstart, x.b);
+            bulk_commit();
+        }
+        return;
+    }
+    const int r0 = rstart + L.g8;
     bool use0 = 16 * wt + L.g8 <= P.a.W + 3, use1 = 16 * wt + L.g8 + 8 <= P.a.W + 3;
     const size_t rb = (size_t)x.b * P.a.T * kHkv + x.g;
     float* p0 = acc_row(P.dk_acc, rb, r0, P.a.T, tig, use0);
@@ -484,7 +535,7 @@ __device__ __forceinline__ void store_dq(const BwdParams& P, const Tile& x, int 
         stsm_x4_t(buf + L.ob[jj], r[2 * jj][0], r[2 * jj][1], r[2 * jj + 1][0], r[2 * jj + 1][1]);
 }
 
-__device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int lane, float* dt_w) {
+__device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int lane, float* dt_w, uint32_t stg) {
     int wcount = 0, gcount = 0, qcount = 0;
     const int u0 = 4 * warp;
     const BLane L = make_blane(lane, u0, P.a.W, P.win_rows);
@@ -505,8 +556,8 @@ __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int la
             __syncwarp();
             mbar_arrive_if(bar_empty_q(S), lane == 0);
             ++qcount;
-            bwd_window_tile<true>(P, S.win, x, u0, 0, L, U);
-            for (int wt = 1; wt < P.nwt; ++wt) bwd_window_tile<false>(P, S.win, x, u0, wt, L, U);
+            bwd_window_tile<true>(P, S.win, x, u0, 0, L, U, stg);
+            for (int wt = 1; wt < P.nwt; ++wt) bwd_window_tile<false>(P, S.win, x, u0, wt, L, U, stg);
             kt = *S.kt;
             __syncwarp();
             mbar_arrive_if(bar_empty_w(S), lane == 0);
@@ -554,11 +605,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_const
     // per consumer warp dL/dt sums, after the output staging buffers
     float* dt_all = reinterpret_cast<float*>(smem_raw + (S.obuf + NCW * kObufBytes - smem_u32(smem_raw)));
     for (int i = threadIdx.x; i < NCW * SFA_MAX_RUNGS; i += blockDim.x) dt_all[i] = 0.f;
+    // per consumer warp 8 KB of window-reduction staging: dK then dV, each two
+    // halves of 32 dimensions x 16 rows in the 128-byte swizzle of the
+    // reduction maps (1024-byte aligned)
+    const uint32_t stg0 = (smem_u32(dt_all + NCW * SFA_MAX_RUNGS) + 1023u) & ~1023u;
     __syncthreads();
     if (warp == NCW) {
         if (lane == 0) producer(P, S);
     } else {
-        bwd_consumer(P, S, warp, lane, dt_all + warp * SFA_MAX_RUNGS);
+        bwd_consumer(P, S, warp, lane, dt_all + warp * SFA_MAX_RUNGS, stg0 + (uint32_t)warp * 8192u);
     }
     __syncthreads();
     if (threadIdx.x < SFA_MAX_RUNGS) {
@@ -702,6 +757,21 @@ size_t bwd_mma_workspace(const LayerArgs& a, bool rope) {
            align256((size_t)kMaxGrid * SFA_MAX_RUNGS * sizeof(float));
 }
 
+// 4-D map over an fp32 accumulator [B][T][2][64] (innermost first: d, head, t,
+// b), box of 32 dimensions x 1 head x 16 positions, 128-byte swizzle: the
+// target of the window tensor reductions.
+static bool encode_red(CUtensorMap* m, const float* base, int B, int T) {
+    auto fn = ring::encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kHkv, (cuuint64_t)T, (cuuint64_t)B};
+    const cuuint64_t strides[3] = {(cuuint64_t)kD * 4, (cuuint64_t)kHkv * kD * 4, (cuuint64_t)T * kHkv * kD * 4};
+    const cuuint32_t box[4] = {32u, 1u, 16u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, const void* v, const void* o,
                            const void* dO, const float* lse, const float2* rope, void* dq, void* dk, void* dv,
                            float* dalpha, float* dtheta, void* ws, unsigned* status, cudaStream_t s) {
@@ -746,6 +816,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.win_region = round1k((unsigned)P.win_rows * ROWB);
     P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) || !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows) ||
+        !encode_red(&P.dkred, P.dk_acc, a.B, a.T) || !encode_red(&P.dvred, P.dv_acc, a.B, a.T) ||
         !encode_out(&P.dqmap, dq, a.B, a.T) || !encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) ||
         !encode_heads(&P.qmaps[1], dO, a.B, a.T, TQ) || !encode_heads(&P.qmaps[2], o, a.B, a.T, TQ))
         return cudaErrorInvalidValue;
@@ -755,7 +826,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
             return cudaErrorInvalidValue;
     }
     const size_t smem = 1024 + kHeaderBytes + BwdParams::kQMaps * (size_t)kQTileBytes + (size_t)P.win_slot_bytes +
-                        NGS * (size_t)kGroupSlotBytes + NCW * (size_t)kObufBytes + kDtBytes;
+                        NGS * (size_t)kGroupSlotBytes + NCW * (size_t)kObufBytes + kDtBytes + 1024 + NCW * 8192;
     static size_t configured_smem[64];
     if (configured_smem[dev & 63] < smem) {
         e = cudaFuncSetAttribute(bwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
