@@ -27,6 +27,10 @@ using sfa::Rung;
 namespace {
 
 constexpr int kMaxT = 1 << 24;  // positions stay exact in fp32
+// B * T cap: every tile, row and thread index of the kernels stays far inside
+// 32 bits, and Q and O alone at this size (512 GiB in bf16) exceed the memory
+// of one GPU, so no shape that fits is turned away.
+constexpr long long kMaxTokens = 1LL << 28;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -44,7 +48,7 @@ sfa_status validate(const sfa_params* p) {
     if (p->dtype != SFA_F32 && p->dtype != SFA_BF16) return SFA_ERR_INVALID_ARG;
     if (p->round_offsets != 0 && p->round_offsets != 1) return SFA_ERR_INVALID_ARG;
     if (p->Hq != sfa::kHq || p->Hkv != sfa::kHkv || p->D != sfa::kD) return SFA_ERR_UNSUPPORTED;
-    if (p->T > kMaxT || (long long)p->B * p->T > 0x7fffffffLL) return SFA_ERR_UNSUPPORTED;
+    if (p->T > kMaxT || (long long)p->B * p->T > kMaxTokens) return SFA_ERR_UNSUPPORTED;
     return SFA_OK;
 }
 

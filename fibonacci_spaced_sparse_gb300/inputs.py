@@ -28,6 +28,24 @@ def normal(shape, *, dtype=torch.bfloat16, seed: int = 42, layer: int = 0,
     return x.to(dtype)
 
 
+def normal_on(device, shape, *, dtype=torch.bfloat16, seed: int = 42, layer: int = 0,
+              stream: str = "q", chunk: int = 1 << 26) -> torch.Tensor:
+    """N(0, 1) draws of ``shape`` made on ``device`` by a generator of that
+    device seeded as above, rounded to ``dtype``: for tensors too large to
+    draw on the host.  Drawn ``chunk`` elements at a time (in order), so the
+    fp32 intermediate stays small; the same arguments give the same tensor on
+    the same device type and PyTorch version, and a test reads back the rows
+    it hands to the oracle."""
+    g = torch.Generator(device=device)
+    g.manual_seed((int(seed) * 1_000_003 + int(layer) * 7_919 + _STREAMS[stream]) % (2 ** 62))
+    out = torch.empty(tuple(shape), dtype=dtype, device=device)
+    flat = out.view(-1)
+    for c in range(0, flat.numel(), chunk):
+        n = min(chunk, flat.numel() - c)
+        flat[c:c + n] = torch.randn((n,), generator=g, device=device, dtype=torch.float32).to(dtype)
+    return out
+
+
 def qkv(B: int, T: int, Hq: int = 8, Hkv: int = 2, D: int = 64, *,
         dtype=torch.bfloat16, seed: int = 42, layer: int = 0, with_dO: bool = False):
     """Q [B,T,Hq,D], K and V [B,T,Hkv,D] (and dO [B,T,Hq,D]) as CPU tensors."""

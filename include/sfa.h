@@ -79,7 +79,8 @@ typedef enum { SFA_F32 = 0, SFA_BF16 = 1 } sfa_dtype;
 #define SFA_DEVSTAT_BAD_INDEX    0x2u  /* a computed row index left [0, T) */
 
 typedef struct {
-    int B, T;          /* batch, sequence length (>= 0; 0 means nothing to do) */
+    int B, T;          /* batch, sequence length (>= 0; 0 means nothing to do);
+                          T <= 2^24 and B * T <= 2^28, else SFA_ERR_UNSUPPORTED */
     int Hq, Hkv, D;    /* heads and head dim; supported: Hq = 8, Hkv = 2, D = 64 */
     int W;             /* window: distances 0..W (W >= 0) */
     int K;             /* number of base offsets, 0 <= K <= SFA_MAX_RUNGS */

@@ -163,6 +163,11 @@ def test_validation_codes(lib):
     assert fwd(_params(), tab=null) == _lib.SFA_ERR_INVALID_ARG    # rope on, no table
     p = _params(T=1 << 25)
     assert fwd(p) == _lib.SFA_ERR_UNSUPPORTED
+    # B * T is capped at 2^28 tokens (the longest sequence, 2^24, times 16)
+    assert fwd(_params(B=17, T=1 << 24)) == _lib.SFA_ERR_UNSUPPORTED
+    assert fwd(_params(B=(1 << 28) + 1, T=1)) == _lib.SFA_ERR_UNSUPPORTED
+    assert lib.sfa_forward_workspace_size(_params(B=17, T=1 << 24).ref()) == 0
+    assert lib.sfa_forward_workspace_size(_params(B=16, T=1 << 24).ref()) == (1 << 28) * 2 * 64 * 2
     assert lib.sfa_forward(None, fake, fake, fake, fake, fake, null, fake, 0, null,
                            null) == _lib.SFA_ERR_INVALID_ARG
     # bf16 needs the rotated-key workspace: too small or misaligned is rejected
