@@ -223,6 +223,27 @@ def recorded_traffic(workload_name):
 
 # ----------------------------------------------------------- CPU baseline --
 
+def host_cpu() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name on x86; implementer
+    and part number on Arm, e.g. 0x41/0xd4f for a Neoverse V2 / Grace core)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip().lower(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "cpu part" in fields:
+        return (f"{platform.machine()} implementer {fields.get('cpu implementer', '?')} "
+                f"part {fields['cpu part']}")
+    return platform.machine() or "unknown"
+
+
 def cpu_baseline(wl, budget_s=12.0):
     """The fp64 oracle as it stands on the host cores: whole layers of the
     workload (all B sequences), cycling through its first four layers until
@@ -249,7 +270,7 @@ def cpu_baseline(wl, budget_s=12.0):
         tokens += wl.B * wl.T
         calls += 1
     return {"value": tokens / spent, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{calls} whole-layer forwards ({wl.B}x{wl.T} query tokens each, "
+            "cpu": host_cpu(), "sample": f"{calls} whole-layer forwards ({wl.B}x{wl.T} query tokens each, "
                       f"layers 0..{nl - 1} in turn), {spent:.1f} s of oracle time"}
 
 
@@ -703,7 +724,7 @@ def run_reference(args, rank, world):
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "W": list(wl.W),
                    "layers": wl.layers, "schedule": wl.schedule, "base": wl.base},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{n_seq} of {wl.B} sequences ({n_seq * wl.T} query tokens) of one "
+                         "cpu": host_cpu(), "sample": f"{n_seq} of {wl.B} sequences ({n_seq * wl.T} query tokens) of one "
                                    f"layer per step, layers 0..{nl - 1} in turn, sized for about "
                                    f"{REFERENCE_BUDGET_S:.0f} s over {warm + steps} steps"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
