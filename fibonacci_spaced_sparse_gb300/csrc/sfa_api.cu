@@ -289,8 +289,8 @@ SFA_API size_t sfa_forward_layers_workspace_size(const sfa_params* p, int L, con
         const size_t n = sfa_forward_workspace_size(&pl);
         if (n > need) need = n;
     }
-    // two rotated-key buffers in turn and one slice counter per layer
-    return layers_batched(p, L, windows) ? 2 * align256_host(need) + align256_host((size_t)L * 4) : need;
+    // two rotated-key buffers, used in turn
+    return layers_batched(p, L, windows) ? 2 * align256_host(need) : need;
 }
 
 SFA_API sfa_status sfa_forward_layers(const sfa_params* p, int L, const float* alphas, const int* windows,
@@ -325,11 +325,9 @@ SFA_API sfa_status sfa_forward_layers(const sfa_params* p, int L, const float* a
         }
         return SFA_OK;
     }
-    const size_t khat_bytes = (need - align256_host((size_t)L * 4)) / 2;
+    const size_t khat_bytes = need / 2;
     char* ws[2] = {static_cast<char*>(workspace), static_cast<char*>(workspace) + khat_bytes};
-    unsigned* counters = reinterpret_cast<unsigned*>(static_cast<char*>(workspace) + 2 * khat_bytes);
     const float2* rope = reinterpret_cast<const float2*>(rope_table);
-    if (cudaMemsetAsync(counters, 0, (size_t)L * 4, stream) != cudaSuccess) return launched(cudaGetLastError());
     LayerArgs a;
     {
         sfa_params pl = *p;
@@ -346,7 +344,7 @@ SFA_API sfa_status sfa_forward_layers(const sfa_params* p, int L, const float* a
         const bool more = l + 1 < L;
         st = launched(sfa::launch_fwd_attention(a, Q[l], ws[l & 1], V[l], rope, O[l], lse ? lse[l] : nullptr,
                                                 more ? K[l + 1] : nullptr, more ? ws[(l + 1) & 1] : nullptr,
-                                                counters + l, status, true, stream));
+                                                status, true, stream));
         if (st != SFA_OK) return st;
     }
     return SFA_OK;

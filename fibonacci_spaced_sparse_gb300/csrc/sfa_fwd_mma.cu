@@ -35,6 +35,9 @@
 //     only when a score exceeds it by more than 2^8) runs over window and
 //     rung entries; O^T accumulates in registers and is transposed with
 //     stmatrix into a staging buffer that a TMA store writes out.
+//     In a multi-layer call each consumer warp also rotates, tile by tile,
+//     the next layer's keys at its four positions (the window slot already
+//     holds their RoPE rows), so that no later layer needs launch 1.
 //
 // Shared memory: each tensor region of a slot is 1024-byte aligned and filled
 // by TMA with the 128-byte swizzle (16-byte chunk c of region row r stored at
@@ -80,7 +83,6 @@ struct FwdParams {
     unsigned* status;
     const __nv_bfloat16* k_next;  // keys of the next layer (multi-layer forward) or nullptr
     __nv_bfloat16* khat_next;     // where their rotated copy goes
-    unsigned* rope_counter;       // slices of k_next handed out so far (zero at launch)
     float sl2;                 // softmax scale x log2(e)
     float inv_sl2;
     int ntq;                   // query tiles per sequence
@@ -509,59 +511,52 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
     }
 }
 
-// Slices of the next layer's RoPE pass (multi-layer forward): slice n is
-// positions 4n .. 4n + 3 of K_next, rotated into Khat_next in the kdim_of
-// order.  Lane = (position p, head g, stored chunk c): it rotates the pairs
-// m = 8 tig + 2c + {0, 1}, tig = 0..3, which fill stored chunks c (x) and
-// 4 + c (y) of the row.  A warp takes kSlices slices at a time from a counter
-// once its tiles are done -- warps of CTAs with fewer tiles take more -- and
-// issues all their loads before it computes.
-constexpr int kSlices = 4;
+// The next layer's RoPE pass (multi-layer forward), done inside the main
+// loop: the consumer warp that owns tile offsets u0 .. u0 + 3 rotates rows
+// i0 + u0 .. i0 + u0 + 3 of K_next (the tile's kv head) into Khat_next, in the
+// kdim_of order, with the RoPE rows of those positions that the window slot
+// already holds.  Tiles cover every (sequence, position, kv head) once, so
+// every row is written once.  Lane = (row r, stored chunk c, half h): it
+// rotates the pairs m = 8 tig + 2c + {0, 1}, tig = 2h, 2h + 1 -- words
+// 4 tig + c (x) and 16 + 4 tig + c (y) of the input row -- and writes words
+// tig = 2h, 2h + 1 of stored chunks c (x) and 4 + c (y).
+struct NextRows {
+    uint32_t xw[2], yw[2];
+    bool ok;
+};
 
-__device__ void rope_tail(const FwdParams& P, int lane) {
-    const int npos = P.a.B * P.a.T;
-    const int nslices = (npos + 3) / 4;
-    const int p = lane >> 3, g = (lane >> 2) & 1, c = lane & 3;
-    for (;;) {
-        unsigned first = 0;
-        if (lane == 0) first = atomicAdd(P.rope_counter, (unsigned)kSlices);
-        first = __shfl_sync(kFull, first, 0);
-        if ((int)first >= nslices) break;
-        float4 t[kSlices][4];
-        uint32_t xw[kSlices][4], yw[kSlices][4];
-        size_t row[kSlices];
-        bool ok[kSlices];
+__device__ __forceinline__ size_t next_row(const FwdParams& P, const Tile& x, int pos) {
+    return ((size_t)x.b * P.a.T + pos) * kHkv + x.g;
+}
+
+__device__ __forceinline__ void load_next_rows(const FwdParams& P, const Tile& x, int u0, int lane, NextRows& N) {
+    const int r = lane >> 3, c = (lane >> 1) & 3, h = lane & 1;
+    const int pos = x.i0 + u0 + r;
+    N.ok = pos < P.a.T;
+    const unsigned* kw = reinterpret_cast<const unsigned*>(P.k_next + next_row(P, x, N.ok ? pos : x.i0) * kD);
 #pragma unroll
-        for (int k = 0; k < kSlices; ++k) {
-            const int pos = 4 * ((int)first + k) + p;
-            ok[k] = pos < npos;
-            const int pc = ok[k] ? pos : npos - 1;
-            row[k] = (size_t)pc * kHkv + g;
-            const unsigned* kw = reinterpret_cast<const unsigned*>(P.k_next + row[k] * kD);
-            const float4* cs = reinterpret_cast<const float4*>(P.rope + (size_t)(pc % P.a.T) * kPairs);
+    for (int j = 0; j < 2; ++j) {
+        N.xw[j] = __ldg(kw + 4 * (2 * h + j) + c);
+        N.yw[j] = __ldg(kw + 16 + 4 * (2 * h + j) + c);
+    }
+}
+
+__device__ __forceinline__ void store_next_rows(const FwdParams& P, const Smem& S, const Tile& x, int u0, int lane,
+                                                const NextRows& N) {
+    const int r = lane >> 3, c = (lane >> 1) & 3, h = lane & 1;
+    const uint32_t trow = S.win + 2 * P.win_region + (uint32_t)((u0 + r) * TABB + 16 * c);
+    uint32_t xo[2], yo[2];
 #pragma unroll
-            for (int tig = 0; tig < 4; ++tig) {
-                // pairs m = 8 tig + 2c + {0, 1}: word 4 tig + c of the row (x), 16 + 4 tig + c (y)
-                t[k][tig] = __ldg(cs + 4 * tig + c);
-                xw[k][tig] = __ldg(kw + 4 * tig + c);
-                yw[k][tig] = __ldg(kw + 16 + 4 * tig + c);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < kSlices; ++k) {
-            uint32_t xo[4], yo[4];
-#pragma unroll
-            for (int tig = 0; tig < 4; ++tig) {
-                const float2 x = unpack_bf16(xw[k][tig]), y = unpack_bf16(yw[k][tig]);
-                xo[tig] = rope_x(x, y, t[k][tig]);
-                yo[tig] = rope_y(x, y, t[k][tig]);
-            }
-            if (ok[k]) {
-                uint4* out = reinterpret_cast<uint4*>(P.khat_next + row[k] * kD);
-                out[c] = make_uint4(xo[0], xo[1], xo[2], xo[3]);
-                out[4 + c] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
-            }
-        }
+    for (int j = 0; j < 2; ++j) {
+        const float4 cs = lds_f4(trow + (uint32_t)(64 * (2 * h + j)));
+        const float2 xv = unpack_bf16(N.xw[j]), yv = unpack_bf16(N.yw[j]);
+        xo[j] = rope_x(xv, yv, cs);
+        yo[j] = rope_y(xv, yv, cs);
+    }
+    if (N.ok) {
+        unsigned char* out = reinterpret_cast<unsigned char*>(P.khat_next + next_row(P, x, x.i0 + u0 + r) * kD);
+        *reinterpret_cast<uint2*>(out + 16 * c + 8 * h) = make_uint2(xo[0], xo[1]);
+        *reinterpret_cast<uint2*>(out + 64 + 16 * c + 8 * h) = make_uint2(yo[0], yo[1]);
     }
 }
 
@@ -572,6 +567,8 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
     const Lane L = make_lane(lane, u0, P.a.W, P.win_rows);
     const uint32_t obuf = S.obuf + (uint32_t)(warp * kObufBytes);
     const int nr = max(P.a.nr, 1);
+    // Khat_next was read by the launch before this one
+    if (P.k_next) asm volatile("griddepcontrol.wait;" ::: "memory");
     Tile x = decode(P, blockIdx.x);
     for (int t = blockIdx.x; t < P.ntiles; t += gridDim.x) {
         Unit U[2];
@@ -585,8 +582,11 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
             __syncwarp();
             mbar_arrive_if(bar_empty_q(S), lane == 0);
             ++qcount;
+            NextRows N;
+            if (P.k_next) load_next_rows(P, x, u0, lane, N);
             window_tile<true>(P, S.win, u0, x.i0, 0, L, U);
             for (int wt = 1; wt < P.nwt; ++wt) window_tile<false>(P, S.win, u0, x.i0, wt, L, U);
+            if (P.k_next) store_next_rows(P, S, x, u0, lane, N);
             kt = *S.kt;
             __syncwarp();
             mbar_arrive_if(bar_empty_w(S), lane == 0);
@@ -608,11 +608,6 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
 #pragma unroll
         for (int k = 0; k < 2; ++k) store_unit(P, x, u0 + 2 * k, obuf, L, lane, U[k]);
         x = next_tile(P, x);
-    }
-    if (P.k_next) {
-        // the buffer written there was read by the launch before this one
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        rope_tail(P, lane);
     }
     if (lane == 0) bulk_wait_all();
     return;
@@ -703,12 +698,13 @@ size_t fwd_mma_workspace(const LayerArgs& a, bool rope) {
 }
 
 // The attention launch of one layer: khat holds the rotated keys (or the raw
-// keys without RoPE); with k_next set it also rotates the next layer's keys
-// into khat_next, handing out slices with *rope_counter (zero at launch).  `after_rope`: the launch directly follows a RoPE pass or
-// an attention launch of this library and may overlap its prologue (PDL).
+// keys without RoPE); with k_next set its consumer warps also rotate the next
+// layer's keys into khat_next, tile by tile.  `pdl`: the launch directly
+// follows a RoPE pass or an attention launch of this library and may overlap
+// its prologue (programmatic dependent launch).
 cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* khat, const void* v,
                                  const float2* rope, void* o, float* lse, const void* k_next, void* khat_next,
-                                 unsigned* rope_counter, unsigned* status, bool pdl, cudaStream_t s) {
+                                 unsigned* status, bool pdl, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -725,8 +721,6 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
     P.rope = rope;
     P.k_next = rope ? static_cast<const __nv_bfloat16*>(k_next) : nullptr;
     P.khat_next = static_cast<__nv_bfloat16*>(khat_next);
-    P.rope_counter = rope_counter;
-    if (P.k_next && !rope_counter) return cudaErrorInvalidValue;
     P.sl2 = a.scale * kLog2e;
     P.inv_sl2 = 1.0f / P.sl2;
     P.ntq = (a.T + TQ - 1) / TQ;
@@ -809,7 +803,7 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
         const cudaError_t e = launch_rope_k(a, k, rope, ws, s);
         if (e != cudaSuccess) return e;
     }
-    return launch_fwd_attention(a, q, rope ? ws : k, v, rope, o, lse, nullptr, nullptr, nullptr, status,
+    return launch_fwd_attention(a, q, rope ? ws : k, v, rope, o, lse, nullptr, nullptr, status,
                                 rope != nullptr, s);
 }
 

@@ -57,7 +57,7 @@ cudaError_t launch_fwd_mma(const LayerArgs& a, const void* q, const void* k, con
 cudaError_t launch_rope_k(const LayerArgs& a, const void* k, const float2* rope, void* khat, cudaStream_t s);
 cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* khat, const void* v,
                                  const float2* rope, void* o, float* lse, const void* k_next, void* khat_next,
-                                 unsigned* rope_counter, unsigned* status, bool pdl, cudaStream_t s);
+                                 unsigned* status, bool pdl, cudaStream_t s);
 
 bool bwd_mma_supported(const LayerArgs& a);
 size_t bwd_mma_workspace(const LayerArgs& a, bool rope);
