@@ -209,33 +209,44 @@ __device__ __forceinline__ float2 bf2(uint32_t w) {
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
-// Rotated (x, y) halves of the 8 pairs of chunk c of a cache row, fp32.
-__device__ __forceinline__ void load_row(const __nv_bfloat16* __restrict__ base, const float2* __restrict__ rope,
-                                         int pos, int c, float (&x)[8], float (&y)[8], float (&v)[16],
-                                         const __nv_bfloat16* __restrict__ vbase) {
-    const uint4 kx = __ldg(reinterpret_cast<const uint4*>(base) + c);
-    const uint4 ky = __ldg(reinterpret_cast<const uint4*>(base) + 4 + c);
-    const uint4 vx = __ldg(reinterpret_cast<const uint4*>(vbase) + c);
-    const uint4 vy = __ldg(reinterpret_cast<const uint4*>(vbase) + 4 + c);
+// The raw words of chunk c of one entry row: Khat dimensions 8c .. 8c + 7 and
+// their partners + 32, the same of V, and the (cos, sin) of those pairs.
+// Fetched for every row of an entry before any of them is used, so that all
+// of an entry's loads are in flight together.
+struct RawRow {
+    uint4 kx, ky, vx, vy;
     float4 cs[4];
+};
+
+__device__ __forceinline__ void fetch_row(const __nv_bfloat16* __restrict__ base,
+                                          const __nv_bfloat16* __restrict__ vbase,
+                                          const float2* __restrict__ rope, int pos, int c, RawRow& R) {
+    R.kx = __ldg(reinterpret_cast<const uint4*>(base) + c);
+    R.ky = __ldg(reinterpret_cast<const uint4*>(base) + 4 + c);
+    R.vx = __ldg(reinterpret_cast<const uint4*>(vbase) + c);
+    R.vy = __ldg(reinterpret_cast<const uint4*>(vbase) + 4 + c);
     if (rope) {
         const float4* t = reinterpret_cast<const float4*>(rope + (size_t)pos * kPairs + 8 * c);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cs[j] = __ldg(t + j);
+        for (int j = 0; j < 4; ++j) R.cs[j] = __ldg(t + j);
     } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) cs[j] = make_float4(1.f, 0.f, 1.f, 0.f);
+        for (int j = 0; j < 4; ++j) R.cs[j] = make_float4(1.f, 0.f, 1.f, 0.f);
     }
-    const uint32_t kxw[4] = {kx.x, kx.y, kx.z, kx.w}, kyw[4] = {ky.x, ky.y, ky.z, ky.w};
-    const uint32_t vxw[4] = {vx.x, vx.y, vx.z, vx.w}, vyw[4] = {vy.x, vy.y, vy.z, vy.w};
+}
+
+// Rotated (x, y) halves of the 8 pairs of a fetched row, and its values, fp32.
+__device__ __forceinline__ void unpack_row(const RawRow& R, float (&x)[8], float (&y)[8], float (&v)[16]) {
+    const uint32_t kxw[4] = {R.kx.x, R.kx.y, R.kx.z, R.kx.w}, kyw[4] = {R.ky.x, R.ky.y, R.ky.z, R.ky.w};
+    const uint32_t vxw[4] = {R.vx.x, R.vx.y, R.vx.z, R.vx.w}, vyw[4] = {R.vy.x, R.vy.y, R.vy.z, R.vy.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const float2 a = bf2(kxw[j]), b = bf2(kyw[j]);
         // pairs 2j, 2j + 1 of the chunk: (cos, sin) in cs[j].xy and cs[j].zw
-        x[2 * j] = a.x * cs[j].x - b.x * cs[j].y;
-        y[2 * j] = b.x * cs[j].x + a.x * cs[j].y;
-        x[2 * j + 1] = a.y * cs[j].z - b.y * cs[j].w;
-        y[2 * j + 1] = b.y * cs[j].z + a.y * cs[j].w;
+        x[2 * j] = a.x * R.cs[j].x - b.x * R.cs[j].y;
+        y[2 * j] = b.x * R.cs[j].x + a.x * R.cs[j].y;
+        x[2 * j + 1] = a.y * R.cs[j].z - b.y * R.cs[j].w;
+        y[2 * j + 1] = b.y * R.cs[j].z + a.y * R.cs[j].w;
         const float2 p = bf2(vxw[j]), q = bf2(vyw[j]);
         v[2 * j] = p.x;
         v[2 * j + 1] = p.y;
@@ -253,8 +264,12 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
     __shared__ float mw[4][kG], lw[4][kG];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x % kHkv, b = blockIdx.x / kHkv;
-    const int i = __ldg(pos + b);
     const size_t qbase = ((size_t)b * kHq + g * kG) * kD;
+    // thread (h, m) rotates pair m of head h of the query; its two values are
+    // loaded together with the position
+    const int qh_h = tid >> 5, qh_m = tid & 31;
+    const __nv_bfloat16 qx_raw = q[qbase + qh_h * kD + qh_m], qy_raw = q[qbase + qh_h * kD + kPairs + qh_m];
+    const int i = __ldg(pos + b);
     if (i < 0 || i >= Tc) {
         // a position outside the cache: report it, read nothing, output zeros
         if (tid == 0 && status) atomicOr(status, SFA_DEVSTAT_BAD_INDEX);
@@ -262,14 +277,6 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
         o[qbase + 2 * tid + 1] = __float2bfloat16_rn(0.f);
         if (lse && tid < kG) lse[(size_t)b * kHq + g * kG + tid] = 0.f;
         return;  // the whole CTA leaves together
-    }
-    // the query: thread (h, m) rotates pair m of head h
-    {
-        const int h = tid >> 5, m = tid & 31;
-        const float x = __bfloat162float(q[qbase + h * kD + m]), y = __bfloat162float(q[qbase + h * kD + kPairs + m]);
-        const float2 cs = rope_cs(rope, i, m);
-        qh[h][m] = x * cs.x - y * cs.y;
-        qh[h][kPairs + m] = y * cs.x + x * cs.y;
     }
     // this lane's entry: window distances 0..min(W, i), then the rungs with
     // ceil(d) <= i (a prefix of the kept list, which is sorted by distance)
@@ -289,15 +296,28 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
     } else if (live) {
         ra = i - e;
     }
-    float kx[8], ky[8], vv[16];
+    // every load of the entry's rows and of the query's (cos, sin) goes out
+    // before any of them is used
+    RawRow A, Bw;
     {
         const size_t off = (((size_t)b * Tc + ra) * kHkv + g) * kD;
-        load_row(kc + off, rope, ra, c, kx, ky, vv, vc + off);
+        fetch_row(kc + off, vc + off, rope, ra, c, A);
     }
     if (rb >= 0) {
-        float bx[8], by[8], bv[16];
         const size_t off = (((size_t)b * Tc + rb) * kHkv + g) * kD;
-        load_row(kc + off, rope, rb, c, bx, by, bv, vc + off);
+        fetch_row(kc + off, vc + off, rope, rb, c, Bw);
+    }
+    {
+        const float x = __bfloat162float(qx_raw), y = __bfloat162float(qy_raw);
+        const float2 cs = rope_cs(rope, i, qh_m);
+        qh[qh_h][qh_m] = x * cs.x - y * cs.y;
+        qh[qh_h][kPairs + qh_m] = y * cs.x + x * cs.y;
+    }
+    float kx[8], ky[8], vv[16];
+    unpack_row(A, kx, ky, vv);
+    if (rb >= 0) {
+        float bx[8], by[8], bv[16];
+        unpack_row(Bw, bx, by, bv);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             kx[j] = wa * kx[j] + wb * bx[j];
