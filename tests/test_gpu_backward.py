@@ -99,3 +99,28 @@ def test_bf16_without_rope_and_many_rungs():
     run(2, 200, "bf16", alpha=0.9, W=8, rope_theta=0.0, layer=8)
     rungs = tuple(range(9, 41))                       # 32 rungs: 8 groups of the ring
     run(1, 240, "bf16", alpha=1.07, W=8, rungs=rungs, layer=9)
+
+
+@pytest.mark.parametrize("dtype,rope", [("bf16", 0.0), ("f32", 1e4)])
+def test_sharp_softmax_gradients(dtype, rope):
+    """Q and K scaled by 6 (scores spread over about 50 log2 units): the
+    recomputed probabilities exp(s - LSE) are close to 0 or 1 and dS is large.
+    bf16 without RoPE, so that both sides score the identical bf16 bytes."""
+    x, _ = draw(2, 300, dtype, layer=32, with_dO=True)
+    for n in ("q", "k"):
+        x[n] = (x[n].float() * 6.0).to(x[n].dtype)
+    f = {n: v.to(torch.float64).numpy() for n, v in x.items()}
+    xd = to_dev(x)
+    kw = dict(alpha=1.21, W=12, rungs=FIB, rope_theta=rope)
+    o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], **kw)
+    dq, dk, dv, da, dth = api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.backward(f["q"], f["k"], f["v"], f["dO"], W=12, rungs=FIB, alpha=1.21, rope_theta=rope)
+    tol = TOL[dtype]
+    for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+        err = max_abs(np64(got), want)
+        bound = tol["grad"] * max(1.0, float(np.abs(want).max()))
+        assert err <= bound, (name, err, bound)
+    # dL/dalpha = sum_k f_k dL/dt_k: the bound scales with sum_k f_k |dL/dt_k|
+    terms = float(np.sum(np.asarray(FIB, dtype=np.float64) * np.abs(ref[5])))
+    assert abs(float(da.item()) - ref[3]) <= tol["dtheta"] * max(terms, abs(ref[3])) + 1e-6

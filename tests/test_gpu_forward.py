@@ -188,3 +188,33 @@ def test_integer_offset_tiles(alpha, W):
 
 def test_integer_offset_tiles_pow2_base():
     check_full(3, 517, "bf16", alpha=1.0, W=8, rungs=api.pow2_base(517), layer=47)
+
+
+# ------------------------------------------------- sharp softmax (rescales) --
+
+
+def _scaled(B, T, dtype, layer, factor, with_dO=False):
+    """Seeded inputs with Q and K multiplied by ``factor`` (rounded once to the
+    dtype), and their exact fp64 copies."""
+    x, _ = draw(B, T, dtype, layer=layer, with_dO=with_dO)
+    for n in ("q", "k"):
+        x[n] = (x[n].float() * factor).to(x[n].dtype)
+    return x, {n: v.to(torch.float64).numpy() for n, v in x.items()}
+
+
+@pytest.mark.parametrize("dtype,rope", [("bf16", 0.0), ("f32", 1e4)])
+def test_sharp_softmax_raises_the_running_max(dtype, rope):
+    """Q and K scaled by 6: scores spread over about 50 log2 units, so the
+    running max is raised many times inside the window and rung tiles (the
+    lazy rescale fires whenever a score beats the max by 2^8).  bf16 runs
+    without RoPE so that both sides score the identical bf16 bytes (with RoPE
+    the kernel rounds the rotated rows to bf16, which moves scores of this size
+    by more than the tolerance)."""
+    x, f = _scaled(2, 300, dtype, 31, 6.0)
+    o, lse = gpu_forward(to_dev(x), alpha=1.21, W=12, rungs=FIB, rope_theta=rope)
+    o_ref, lse_ref = oracle.forward(f["q"], f["k"], f["v"], W=12, rungs=FIB, alpha=1.21,
+                                    rope_theta=rope)
+    # the reference itself is sharp: most rows put over half their weight on one entry
+    assert float(np.median(lse_ref)) > 30.0
+    assert max_abs(np64(o), o_ref) <= TOL[dtype]["o"]
+    assert max_abs(np64(lse), lse_ref) <= TOL[dtype]["lse"] * max(1.0, float(np.abs(lse_ref).max()) / 100)
