@@ -12,10 +12,10 @@
 //   dL/dt += scale ds (qhat . khat_b - qhat . khat_a) + p (dO . v_b - dO . v_a),
 // dL/dalpha = sum_k f_k dL/dt_k, dL/dtheta = dL/dalpha (alpha - 0.5)(1.5 - alpha).
 //
-// Three launches and a memset:
-//  0. the fp32 dKhat / dV accumulators are zeroed (cudaMemsetAsync).
-//  1. bwd_prep_kernel: Khat = RoPE(K) (bf16, natural dimension order) into the
-//     workspace (not launched when the inputs come rotated).
+// Three launches, the last two as programmatic dependents of the one before:
+//  1. bwd_prep_kernel: zeroes the fp32 dKhat / dV accumulators and writes
+//     Khat = RoPE(K) (bf16, natural dimension order) into the workspace (the
+//     rotation is skipped when the inputs come rotated).
 //  2. bwd_mma_kernel: persistent, the forward's tile map and load ring (one
 //     producer lane, seven consumer warps, a warp owns a quad of queries as
 //     two pairs).  Per M tile ("keys on M", as in the forward) it recomputes
@@ -31,8 +31,8 @@
 //     registers and go to the accumulators with red.global.add.v2.  dQ is
 //     rotated back (R(i)^T) and stored through shared memory by TMA; dL/dt is
 //     summed per warp in shared memory and per CTA into the workspace.
-//  3. bwd_finish_kernel: dK = R(j)^T dKhat and dV to the caller's dtype, and
-//     the fixed-order (fp64) reduction of dL/dalpha and dL/dtheta.
+//  3. bwd_finish_mma_kernel: dK = R(j)^T dKhat and dV to the caller's dtype,
+//     and the fixed-order (fp64) reduction of dL/dalpha and dL/dtheta.
 #include <cstring>
 
 #include "sfa_internal.cuh"
@@ -600,6 +600,9 @@ fail:
 
 __global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_constant__ BwdParams P) {
     extern __shared__ unsigned char smem_raw[];
+    // the finish kernel may be scheduled now; it waits for this grid before it
+    // reads anything
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const Smem S = ring_setup(P.a, NCW, BwdParams::kQMaps * kQTileBytes, P.win_slot_bytes, smem_raw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // per consumer warp dL/dt sums, after the output staging buffers
@@ -625,16 +628,31 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_const
 
 // ------------------------------------------------------ prep and finish
 
+// Zeroes the fp32 dK-hat and dV accumulators and, with a RoPE table, writes
 // Khat = RoPE(K) in the natural dimension order.  Four threads per row
-// (b, j, g): thread a takes the rotation pairs 8a .. 8a + 7.
+// (b, j, g): thread a zeroes dimensions 16a .. 16a + 15 of the row in both
+// accumulators and takes the rotation pairs 8a .. 8a + 7.
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloat16* __restrict__ k,
                                                                 const float2* __restrict__ rope,
-                                                                __nv_bfloat16* __restrict__ khat, unsigned rows,
+                                                                __nv_bfloat16* __restrict__ khat,
+                                                                float* __restrict__ dk_acc,
+                                                                float* __restrict__ dv_acc, unsigned rows,
                                                                 unsigned T) {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const unsigned idx = blockIdx.x * kPrepThreads + threadIdx.x;
     const unsigned row = idx >> 2, a = idx & 3;
     if (row >= rows) return;
+    {
+        float4* zk = reinterpret_cast<float4*>(dk_acc + (size_t)row * kD + 16 * a);
+        float4* zv = reinterpret_cast<float4*>(dv_acc + (size_t)row * kD + 16 * a);
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            zk[c] = z;
+            zv[c] = z;
+        }
+    }
+    if (!rope) return;
     const unsigned j = (row / kHkv) % T;
     const __nv_bfloat16* kr = k + (size_t)row * kD;
     const uint4 xv = __ldg(reinterpret_cast<const uint4*>(kr + 8 * a));
@@ -663,6 +681,8 @@ __global__ void __launch_bounds__(kFinishThreads) bwd_finish_mma_kernel(
     const float2* __restrict__ rope, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
     const float* __restrict__ dt_part, int nparts, float* __restrict__ dalpha, float* __restrict__ dtheta,
     unsigned rows) {
+    // launched as a dependent of the main kernel: its results must be complete
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (blockIdx.x == 0) {
         __shared__ double per_rung[SFA_MAX_RUNGS];
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -782,14 +802,11 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     if (e != cudaSuccess) return e;
     const BwdWorkspace w = carve(a, rope != nullptr, ws);
     const unsigned rows = (unsigned)a.B * (unsigned)a.T * kHkv;
-    // the two fp32 accumulators are contiguous
-    e = cudaMemsetAsync(w.dk_acc, 0, (size_t)(reinterpret_cast<char*>(w.dt_part) - reinterpret_cast<char*>(w.dk_acc)),
-                        s);
-    if (e != cudaSuccess) return e;
-    if (rope) {
+    {
+        // zeroes the accumulators (and rotates K with RoPE on)
         const unsigned blocks = (rows * 4 + kPrepThreads - 1) / kPrepThreads;
-        bwd_prep_kernel<<<blocks, kPrepThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k), rope, w.khat, rows,
-                                                        (unsigned)a.T);
+        bwd_prep_kernel<<<blocks, kPrepThreads, 0, s>>>(static_cast<const __nv_bfloat16*>(k), rope, w.khat,
+                                                        w.dk_acc, w.dv_acc, rows, (unsigned)a.T);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         count_launch();
     }
@@ -861,16 +878,23 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = rope ? 1 : 0;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, bwd_mma_kernel, P);
     if (e != cudaSuccess) return e;
     count_launch();
     {
         const unsigned row_blocks = (rows * 4 + kFinishThreads - 1) / kFinishThreads;
-        bwd_finish_mma_kernel<<<row_blocks + 1, kFinishThreads, 0, s>>>(
-            a, w.dk_acc, w.dv_acc, rope, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-            w.dt_part, (int)grid, dalpha, dtheta, rows);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        cudaLaunchConfig_t fc = {};
+        fc.gridDim = dim3(row_blocks + 1);
+        fc.blockDim = dim3(kFinishThreads);
+        fc.dynamicSmemBytes = 0;
+        fc.stream = s;
+        fc.attrs = attr;
+        fc.numAttrs = 1;
+        e = cudaLaunchKernelEx(&fc, bwd_finish_mma_kernel, a, (const float*)w.dk_acc, (const float*)w.dv_acc,
+                               rope, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+                               (const float*)w.dt_part, (int)grid, dalpha, dtheta, rows);
+        if (e != cudaSuccess) return e;
         count_launch();
     }
     return cudaSuccess;

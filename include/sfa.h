@@ -315,10 +315,10 @@ SFA_API size_t sfa_backward_workspace_size(const sfa_params *p);
  *     bytes, contents ignored on entry and clobbered;
  *   status: device word or NULL.
  * The derivative of floor/ceil and of the drop and mask decisions is zero.
- * Asynchronous on stream.  bf16 with W <= 30: a memset of the fp32
- * accumulators, a RoPE launch over K (skipped when rope_theta <= 0), the
- * tensor-core kernel and a finish launch; fp32 and wider windows: three
- * launches of the fp32-arithmetic kernels. */
+ * Asynchronous on stream.  bf16 with W <= 30: three launches (one that
+ * zeroes the fp32 accumulators in the workspace and rotates K, the rotation
+ * skipped when rope_theta <= 0; the tensor-core kernel; a finish launch);
+ * fp32 and wider windows: three launches of the fp32-arithmetic kernels. */
 SFA_API sfa_status sfa_backward(const sfa_params *p, const void *Q, const void *K,
                                 const void *V, const void *O, const void *dO,
                                 const float *lse, const float *rope_table, void *dQ,
