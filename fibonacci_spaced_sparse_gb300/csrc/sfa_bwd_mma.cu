@@ -629,9 +629,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) bwd_mma_kernel(const __grid_const
 // ------------------------------------------------------ prep and finish
 
 // Zeroes the fp32 dK-hat and dV accumulators and, with a RoPE table, writes
-// Khat = RoPE(K) in the natural dimension order.  Four threads per row
-// (b, j, g): thread a zeroes dimensions 16a .. 16a + 15 of the row in both
-// accumulators and takes the rotation pairs 8a .. 8a + 7.
+// Khat = RoPE(K) in the natural dimension order.  Thread idx of the 4 rows
+// threads zeroes the 16-byte words idx + n * 4 rows (n = 0..3) of each
+// accumulator (a warp's stores cover 512 contiguous bytes); for the rotation
+// four threads take a row (b, j, g), thread a the pairs 8a .. 8a + 7.
 __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloat16* __restrict__ k,
                                                                 const float2* __restrict__ rope,
                                                                 __nv_bfloat16* __restrict__ khat,
@@ -643,13 +644,14 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
     const unsigned row = idx >> 2, a = idx & 3;
     if (row >= rows) return;
     {
-        float4* zk = reinterpret_cast<float4*>(dk_acc + (size_t)row * kD + 16 * a);
-        float4* zv = reinterpret_cast<float4*>(dv_acc + (size_t)row * kD + 16 * a);
+        const size_t nthreads = (size_t)rows * 4;
+        float4* zk = reinterpret_cast<float4*>(dk_acc) + idx;
+        float4* zv = reinterpret_cast<float4*>(dv_acc) + idx;
         const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            zk[c] = z;
-            zv[c] = z;
+        for (int n = 0; n < 4; ++n) {
+            zk[n * nthreads] = z;
+            zv[n * nthreads] = z;
         }
     }
     if (!rope) return;
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
     *reinterpret_cast<uint4*>(out + 32 + 8 * a) = make_uint4(yo[0], yo[1], yo[2], yo[3]);
 }
 
-// dK = R(j)^T dKhat and dV, bf16, four threads per row (pairs 8a .. 8a + 7).
+// dK = R(j)^T dKhat and dV, bf16, eight threads per row (pairs 4q .. 4q + 3).
 // Block 0 reduces dL/dt over the CTA partials instead: warp w takes the rungs
 // w, w + 8, ..., lanes sum strided partials in fp64 and a fixed-order
 // butterfly finishes each rung, so the result does not depend on timing.
@@ -704,41 +706,33 @@ __global__ void __launch_bounds__(kFinishThreads) bwd_finish_mma_kernel(
         }
         return;
     }
-    const unsigned idx = (blockIdx.x - 1) * kFinishThreads + threadIdx.x;
-    const unsigned row = idx >> 2, q = idx & 3;
+    // eight threads per row: thread q takes dimensions 4q .. 4q + 3 and their
+    // rotation partners 32 + 4q .. 32 + 4q + 3 (a warp's loads cover 128
+    // contiguous bytes of a row half, its stores 64)
+    const size_t idx = (size_t)(blockIdx.x - 1) * kFinishThreads + threadIdx.x;
+    const size_t row = idx >> 3;
+    const int q = (int)(idx & 7);
     if (row >= rows) return;
-    const float4* xk = reinterpret_cast<const float4*>(dk_acc + (size_t)row * kD + 8 * q);
-    const float4* yk = reinterpret_cast<const float4*>(dk_acc + (size_t)row * kD + 32 + 8 * q);
-    const float4* xv = reinterpret_cast<const float4*>(dv_acc + (size_t)row * kD + 8 * q);
-    const float4* yv = reinterpret_cast<const float4*>(dv_acc + (size_t)row * kD + 32 + 8 * q);
-    float x[8], y[8];
-    *reinterpret_cast<float4*>(x) = xk[0];
-    *reinterpret_cast<float4*>(x + 4) = xk[1];
-    *reinterpret_cast<float4*>(y) = yk[0];
-    *reinterpret_cast<float4*>(y + 4) = yk[1];
+    const size_t base = row * kD + 4 * q;
+    float4 x = *reinterpret_cast<const float4*>(dk_acc + base);
+    float4 y = *reinterpret_cast<const float4*>(dk_acc + base + 32);
+    const float4 vx = *reinterpret_cast<const float4*>(dv_acc + base);
+    const float4 vy = *reinterpret_cast<const float4*>(dv_acc + base + 32);
     if (rope) {
-        const unsigned j = (row / kHkv) % (unsigned)a.T;
-        const float4* cs = reinterpret_cast<const float4*>(rope + (size_t)j * kPairs + 8 * q);
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            const float4 t = __ldg(cs + c);
-            const float x0 = x[2 * c], x1 = x[2 * c + 1], y0 = y[2 * c], y1 = y[2 * c + 1];
-            x[2 * c] = t.x * x0 + t.y * y0;
-            y[2 * c] = t.x * y0 - t.y * x0;
-            x[2 * c + 1] = t.z * x1 + t.w * y1;
-            y[2 * c + 1] = t.z * y1 - t.w * x1;
-        }
+        const unsigned j = (unsigned)((row / kHkv) % (unsigned)a.T);
+        const float4* cs = reinterpret_cast<const float4*>(rope + (size_t)j * kPairs + 4 * q);
+        // pairs 4q, 4q + 1 in t0 and 4q + 2, 4q + 3 in t1: (cos, sin) each
+        const float4 t0 = __ldg(cs), t1 = __ldg(cs + 1);
+        const float4 x0 = x, y0 = y;
+        x = make_float4(t0.x * x0.x + t0.y * y0.x, t0.z * x0.y + t0.w * y0.y, t1.x * x0.z + t1.y * y0.z,
+                        t1.z * x0.w + t1.w * y0.w);
+        y = make_float4(t0.x * y0.x - t0.y * x0.x, t0.z * y0.y - t0.w * x0.y, t1.x * y0.z - t1.y * x0.z,
+                        t1.z * y0.w - t1.w * x0.w);
     }
-    uint4 ko0, ko1, vo0, vo1;
-    ko0 = make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
-    ko1 = make_uint4(pack_bf16(y[0], y[1]), pack_bf16(y[2], y[3]), pack_bf16(y[4], y[5]), pack_bf16(y[6], y[7]));
-    const float4 v0 = xv[0], v1 = xv[1], v2 = yv[0], v3 = yv[1];
-    vo0 = make_uint4(pack_bf16(v0.x, v0.y), pack_bf16(v0.z, v0.w), pack_bf16(v1.x, v1.y), pack_bf16(v1.z, v1.w));
-    vo1 = make_uint4(pack_bf16(v2.x, v2.y), pack_bf16(v2.z, v2.w), pack_bf16(v3.x, v3.y), pack_bf16(v3.z, v3.w));
-    *reinterpret_cast<uint4*>(dk + (size_t)row * kD + 8 * q) = ko0;
-    *reinterpret_cast<uint4*>(dk + (size_t)row * kD + 32 + 8 * q) = ko1;
-    *reinterpret_cast<uint4*>(dv + (size_t)row * kD + 8 * q) = vo0;
-    *reinterpret_cast<uint4*>(dv + (size_t)row * kD + 32 + 8 * q) = vo1;
+    *reinterpret_cast<uint2*>(dk + base) = make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+    *reinterpret_cast<uint2*>(dk + base + 32) = make_uint2(pack_bf16(y.x, y.y), pack_bf16(y.z, y.w));
+    *reinterpret_cast<uint2*>(dv + base) = make_uint2(pack_bf16(vx.x, vx.y), pack_bf16(vx.z, vx.w));
+    *reinterpret_cast<uint2*>(dv + base + 32) = make_uint2(pack_bf16(vy.x, vy.y), pack_bf16(vy.z, vy.w));
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -883,7 +877,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     if (e != cudaSuccess) return e;
     count_launch();
     {
-        const unsigned row_blocks = (rows * 4 + kFinishThreads - 1) / kFinishThreads;
+        const unsigned row_blocks = (unsigned)(((size_t)rows * 8 + kFinishThreads - 1) / kFinishThreads);
         cudaLaunchConfig_t fc = {};
         fc.gridDim = dim3(row_blocks + 1);
         fc.blockDim = dim3(kFinishThreads);
