@@ -26,7 +26,8 @@ def _check(got, want):
     assert err.max() <= 0, float(np.max(np.abs(g - want)))
 
 
-@pytest.mark.parametrize("B,T,dm", [(2, 300, 512), (1, 5, 64), (3, 97, 192), (1, 256, 1024)])
+@pytest.mark.parametrize("B,T,dm", [(2, 300, 512), (1, 5, 64), (3, 97, 192), (1, 256, 1024), (2, 150, 320),
+                                     (1, 40, 16384)])
 @pytest.mark.parametrize("rope_theta", [1e4, 0.0])
 def test_front_end_against_oracle(B, T, dm, rope_theta):
     x, w, xf, wf = _draw(B, T, dm, layer=B * 7 + dm)
