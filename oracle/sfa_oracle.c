@@ -12,7 +12,8 @@
  *   - "Attended set": query i attends the dense window of distances 0..W
  *     (self included) plus one rung per base offset f_k at the continuous
  *     distance d_k = alpha * f_k; each rung reads the key/value row at i - d_k by
- *     linear interpolation between the floor and floor+1 distances; RoPE is
+ *     linear interpolation of the rows at the whole distances just below and
+ *     just above d_k; RoPE is
  *     applied at the true positions before the gather; the offset set is the
  *     same for every query.
  *   - "Per-layer scalar": alpha = 0.5 + sigmoid(theta), theta the only added
@@ -39,7 +40,7 @@
  *     rope_theta^(-2m/D); rope_theta <= 0 means no rotation;
  *   - query head h reads key/value head h / (Hq/Hkv);
  *   - the derivative of floor/ceil and of the drop/mask decisions is zero, and
- *     at t = 0 the t-derivative of an entry whose row floor+1 lies before the
+ *     at t = 0 the t-derivative of an entry whose far row (distance n + 1) lies before the
  *     sequence start is zero (that row does not exist).
  *
  * Layout of every tensor: row-major [B][T][H][D], D fastest, fp64.

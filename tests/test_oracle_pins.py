@@ -185,7 +185,7 @@ def test_alpha1_dense_mask_batched(W):
 
 def test_lerp_limit_from_below_is_plain_gather():
     """As alpha -> 1 from below, each rung's fraction t -> 1 and the lerp tends
-    to the plain gather of row i - f_k (weight t on row floor+1 distance)."""
+    to the plain gather of row i - f_k (weight t on the row at distance n + 1)."""
     x = _inputs(1, 200, layer=1)
     W = 8
     eps = 2.0 ** -32
