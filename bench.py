@@ -409,15 +409,18 @@ def run_ours(args, rank, world, local):
 def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
     """Same step through the C ABI from pinned host buffers: each step copies
     every layer's Q, K, V host->device, runs the layer, and copies O back.
-    Copies run on their own streams so that layer l's attention overlaps the
-    upload of layer l+1 and the download of layer l-1 (double-buffered device
-    staging); events order each layer's three stages."""
+    Copies run on their own streams through NB device staging buffers used in
+    turn (across steps too), so the uploads run ahead of the attention and the
+    downloads follow it; events order each layer's three stages.  The only
+    waits are the hazards: an upload into a buffer waits for the attention
+    launch that last read it, an attention launch waits for the download that
+    last read its output buffer."""
     import torch
     from fibonacci_spaced_sparse_gb300 import api
     L = wl.layers
     pin = [{k: host[l][k].pin_memory() for k in ("q", "k", "v")} for l in range(L)]
     o_host = [torch.empty_like(pin[l]["q"]).pin_memory() for l in range(L)]
-    NB = 2
+    NB = 3
     dq = [{k: torch.empty_like(pin[0][k], device=dev) for k in ("q", "k", "v")} for _ in range(NB)]
     do = [torch.empty_like(dq[0]["q"]) for _ in range(NB)]
     lse = [torch.empty((wl.B, wl.T, 8), dtype=torch.float32, device=dev) for _ in range(NB)]
@@ -425,43 +428,50 @@ def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
     d2h = sum(o.numel() * o.element_size() for o in o_host)
     up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()
+    read_in = [None] * NB    # per buffer: the attention launch that last read its inputs
+    read_out = [None] * NB   # per buffer: the download that last read its output
+    turn = [0]
 
     def step():
-        loaded = [None] * L
-        computed = [None] * L
-        freed = [None] * NB      # buffer may be overwritten once its O was downloaded
         for l in range(L):
-            s = l % NB
+            s = turn[0] % NB
+            turn[0] += 1
             with torch.cuda.stream(up):
-                if freed[s] is not None:
-                    up.wait_event(freed[s])
-                if l >= NB and computed[l - NB] is not None:
-                    up.wait_event(computed[l - NB])   # inputs of layer l-NB consumed
+                if read_in[s] is not None:
+                    up.wait_event(read_in[s])
                 for k in ("q", "k", "v"):
                     dq[s][k].copy_(pin[l][k], non_blocking=True)
-                loaded[l] = ev()
-                loaded[l].record(up)
-            stream.wait_event(loaded[l])
+                loaded = ev()
+                loaded.record(up)
+            stream.wait_event(loaded)
+            if read_out[s] is not None:
+                stream.wait_event(read_out[s])
             api.sfa_forward(dq[s]["q"], dq[s]["k"], dq[s]["v"], alpha=alphas[l], W=wl.window(l),
                             rungs=wl.rungs(), out=do[s], lse=lse[s], stream=stream)
-            computed[l] = ev()
-            computed[l].record(stream)
+            read_in[s] = ev()
+            read_in[s].record(stream)
             with torch.cuda.stream(down):
-                down.wait_event(computed[l])
+                down.wait_event(read_in[s])
                 o_host[l].copy_(do[s], non_blocking=True)
-                freed[s] = ev()
-                freed[s].record(down)
+                read_out[s] = ev()
+                read_out[s].record(down)
+
+    def drain():
         stream.wait_stream(up)
         stream.wait_stream(down)
 
     for _ in range(max(3, min(args.warmup, 5))):
         step()
+    drain()
     torch.cuda.synchronize(dev)
     steps = min(args.steps, E2E_MAX_STEPS)  # each step moves 1.3 GB over the host link
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
+    up.wait_stream(stream)
+    down.wait_stream(stream)
     for _ in range(steps):
         step()
+    drain()
     stop.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(start.elapsed_time(stop), dev)
