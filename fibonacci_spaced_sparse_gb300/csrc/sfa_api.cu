@@ -19,6 +19,18 @@ namespace sfa {
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Test hook: SFA_TEST_FAULT=launch in the environment (read once) makes every
+// entry point fail with SFA_ERR_CUDA after its argument checks, before it
+// touches the GPU, so that callers' error paths can be exercised without a
+// device fault.
+bool fault_injected() {
+    static const bool on = [] {
+        const char* e = std::getenv("SFA_TEST_FAULT");
+        return e && std::strcmp(e, "launch") == 0;
+    }();
+    return on;
+}
+
 }  // namespace sfa
 
 using sfa::LayerArgs;
@@ -247,6 +259,7 @@ SFA_API sfa_status sfa_rope_table(float* table, int T, int D, float rope_theta,
         !std::isfinite(rope_theta) || !(rope_theta > 0.f))
         return SFA_ERR_INVALID_ARG;
     if (T == 0) return SFA_OK;
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     return launched(sfa::launch_rope_table(reinterpret_cast<float2*>(table), T, D,
                                            (double)rope_theta, stream));
 }
@@ -272,9 +285,11 @@ SFA_API sfa_status sfa_forward(const sfa_params* p, const void* Q, const void* K
         if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) ||
                      workspace_bytes < need))
             return SFA_ERR_INVALID_ARG;
+        if (sfa::fault_injected()) return SFA_ERR_CUDA;
         return launched(sfa::launch_fwd_mma(a, Q, K, V, rope_ptr(p, rope_table), O, lse, workspace,
                                             status, stream));
     }
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     return launched(sfa::launch_fwd_simple(a, p->dtype, Q, K, V, rope_ptr(p, rope_table), O, lse,
                                            stream));
 }
@@ -314,6 +329,7 @@ SFA_API sfa_status sfa_forward_layers(const sfa_params* p, int L, const float* a
     const size_t need = sfa_forward_layers_workspace_size(p, L, windows);
     if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need))
         return SFA_ERR_INVALID_ARG;
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     if (!layers_batched(p, L, windows)) {
         for (int l = 0; l < L; ++l) {
             sfa_params pl = *p;
@@ -361,6 +377,7 @@ SFA_API sfa_status sfa_decode(const sfa_params* p, const void* Q, const void* Kc
     if (!positions || (reinterpret_cast<uintptr_t>(positions) & 3u)) return SFA_ERR_INVALID_ARG;
     LayerArgs a;
     fill_args(p, &a);
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     return launched(sfa::launch_decode(a, p->T, p->dtype, Q, Kc, Vc, positions, rope_ptr(p, rope_table), O,
                                        lse, status, stream));
 }
@@ -378,12 +395,14 @@ SFA_API sfa_status sfa_qkv_rope(const sfa_params* p, int d_model, const void* X,
         !aligned16(Khat) || !aligned16(V))
         return SFA_ERR_INVALID_ARG;
     if (p->rope_theta > 0.f && (!rope_table || !aligned16(rope_table))) return SFA_ERR_INVALID_ARG;
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     return launched(sfa::launch_qkv_rope((int)M, p->T, d_model, X, Wqkv, rope_ptr(p, rope_table), Qhat, Khat,
                                          V, status, stream));
 }
 
 SFA_API sfa_status sfa_selftest_wait_timeout(unsigned int* status, cudaStream_t stream) {
     if (!status || (reinterpret_cast<uintptr_t>(status) & 3u)) return SFA_ERR_INVALID_ARG;
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     return launched(sfa::launch_wait_selftest(status, stream));
 }
 
@@ -408,6 +427,7 @@ SFA_API sfa_status sfa_backward(const sfa_params* p, const void* Q, const void* 
     LayerArgs a;
     fill_args(p, &a);
     if (p->B == 0 || p->T == 0) {
+        if (sfa::fault_injected()) return SFA_ERR_CUDA;
         if (cudaMemsetAsync(dalpha, 0, sizeof(float), stream) != cudaSuccess ||
             cudaMemsetAsync(dtheta, 0, sizeof(float), stream) != cudaSuccess)
             return launched(cudaGetLastError());
@@ -422,6 +442,7 @@ SFA_API sfa_status sfa_backward(const sfa_params* p, const void* Q, const void* 
     const size_t need = mma ? sfa::bwd_mma_workspace(a, p->rope_theta > 0.f) : sfa::bwd_simple_workspace(a);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < need)
         return SFA_ERR_INVALID_ARG;
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     if (mma)
         return launched(sfa::launch_bwd_mma(a, Q, K, V, O, dO, lse, rope_ptr(p, rope_table), dQ, dK, dV,
                                             dalpha, dtheta, workspace, status, stream));
@@ -432,6 +453,7 @@ SFA_API sfa_status sfa_backward(const sfa_params* p, const void* Q, const void* 
 SFA_API sfa_status sfa_read_status(const unsigned int* status, unsigned int* host_word,
                                    cudaStream_t stream) {
     if (!status) return SFA_ERR_INVALID_ARG;
+    if (sfa::fault_injected()) return SFA_ERR_CUDA;
     unsigned int w = 0;
     if (cudaMemcpyAsync(&w, status, sizeof(w), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
         cudaStreamSynchronize(stream) != cudaSuccess) {

@@ -41,6 +41,9 @@ struct LayerArgs {
 
 // Host: count of kernel launches made by the library.
 void count_launch();
+// SFA_TEST_FAULT=launch in the environment: entry points fail with
+// SFA_ERR_CUDA after their argument checks, before they launch anything.
+bool fault_injected();
 
 // Launchers (each returns the launch error, if any).
 cudaError_t launch_rope_table(float2* table, int T, int D, double theta, cudaStream_t s);

@@ -45,6 +45,14 @@
  * sets a bit in the optional device status word (see SFA_DEVSTAT_*) and
  * returns; sfa_read_status() turns a non-zero word into SFA_ERR_DEVICE_STATUS.
  * Outputs are undefined after any error.
+ *
+ * Test hook.  With SFA_TEST_FAULT=launch in the environment (read once per
+ * process) every entry point that would launch work or read the status word
+ * checks its arguments as usual and then returns SFA_ERR_CUDA without
+ * launching, so that a caller's error handling can be exercised without
+ * faulting a GPU.  Calls with nothing to launch (B * T = 0) still return
+ * SFA_OK, except sfa_backward, which then still zeroes dalpha and dtheta and
+ * so fails too.
  */
 #ifndef SFA_H
 #define SFA_H

@@ -1,7 +1,9 @@
 """Failure detection without a GPU fault: a pipeline wait that nothing
 satisfies gives up after its limit, the kernel reports
 SFA_DEVSTAT_WAIT_TIMEOUT in the status word and returns, and the context
-stays usable (a forward afterwards still matches the oracle)."""
+stays usable (a forward afterwards still matches the oracle); a launch
+failure injected on the host (SFA_TEST_FAULT=launch) reaches the Python
+caller as an exception with nothing launched."""
 import time
 
 import numpy as np
@@ -40,3 +42,33 @@ def test_clean_runs_leave_the_status_word_clear():
     o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], alpha=1.1, W=12, status=status)
     api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse, alpha=1.1, W=12, status=status)
     assert api.sfa_read_status(status) == 0
+
+
+def test_injected_launch_fault_raises_in_the_binding():
+    """SFA_TEST_FAULT=launch (a host-side hook, no device fault): the Python
+    binding raises on the library's SFA_ERR_CUDA and no kernel is launched."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = r"""
+import json, torch
+from fibonacci_spaced_sparse_gb300 import api
+q = torch.randn(1, 64, 8, 64, device="cuda").bfloat16()
+k = torch.randn(1, 64, 2, 64, device="cuda").bfloat16()
+v = torch.randn(1, 64, 2, 64, device="cuda").bfloat16()
+n0 = api.launch_count()
+try:
+    api.sfa_forward(q, k, v, alpha=1.0, W=12, rope_theta=0.0)
+    raised = ""
+except RuntimeError as e:
+    raised = str(e)
+print(json.dumps({"raised": raised, "launches": api.launch_count() - n0}))
+"""
+    env = dict(os.environ, SFA_TEST_FAULT="launch", PYTHONPATH=root)
+    r = subprocess.run([sys.executable, "-c", code], env=env, cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr
+    got = json.loads(r.stdout.strip().splitlines()[-1])
+    assert got["raised"] and got["launches"] == 0, got
