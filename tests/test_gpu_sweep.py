@@ -14,7 +14,7 @@ from _helpers import TOL, draw, max_abs, np64, to_dev
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 24
+N_CASES = 48
 
 
 def _case(seed):
