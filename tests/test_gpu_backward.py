@@ -124,3 +124,21 @@ def test_sharp_softmax_gradients(dtype, rope):
     # dL/dalpha = sum_k f_k dL/dt_k: the bound scales with sum_k f_k |dL/dt_k|
     terms = float(np.sum(np.asarray(FIB, dtype=np.float64) * np.abs(ref[5])))
     assert abs(float(da.item()) - ref[3]) <= tol["dtheta"] * max(terms, abs(ref[3])) + 1e-6
+
+
+@pytest.mark.parametrize("dtype,scale", [("bf16", 0.05), ("bf16", 0.3), ("f32", 0.2)])
+def test_explicit_softmax_scale_gradients(dtype, scale):
+    """dQ, dK, dV and dL/dalpha with a caller-given softmax scale."""
+    x, f = draw(2, 150, dtype, layer=62, with_dO=True)
+    xd = to_dev(x)
+    kw = dict(alpha=0.83, W=12, rungs=FIB, scale=scale)
+    o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], **kw)
+    dq, dk, dv, da, dth = api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse, **kw)
+    torch.cuda.synchronize()
+    ref = oracle.backward(f["q"], f["k"], f["v"], f["dO"], W=12, rungs=FIB, alpha=0.83, scale=scale)
+    tol = TOL[dtype]
+    for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
+        bound = tol["grad"] * max(1.0, float(np.abs(want).max()))
+        assert max_abs(np64(got), want) <= bound, name
+    terms = float(np.sum(np.asarray(FIB, dtype=np.float64) * np.abs(ref[5])))
+    assert abs(float(da.item()) - ref[3]) <= tol["dtheta"] * max(terms, abs(ref[3])) + 1e-6

@@ -93,3 +93,19 @@ def test_decode_long_key_lists(alpha, W):
     """Key lists longer than 32 entries (W = 24, 30) take the general kernel,
     shorter ones the one-pass kernel; both against the oracle."""
     _case(16, 1200, "bf16", alpha, W, seed=7)
+
+
+def test_decode_explicit_softmax_scale():
+    B, Tc = 6, 400
+    x, _ = draw(B, Tc, "bf16", layer=63)
+    pos = np.array([0, 7, 13, 150, 398, 399], dtype=np.int32)
+    qd = torch.stack([x["q"][b, p] for b, p in enumerate(pos)])
+    o, lse = api.sfa_decode(qd.cuda(), x["k"].cuda(), x["v"].cuda(), torch.from_numpy(pos).cuda(),
+                            alpha=1.2, W=12, rungs=FIB, scale=0.3)
+    torch.cuda.synchronize()
+    rows = np.stack([np.arange(B, dtype=np.int32), pos], axis=1)
+    f = {n: x[n].to(torch.float64).numpy() for n in ("q", "k", "v")}
+    o_ref, lse_ref = oracle.forward_rows(f["q"], f["k"], f["v"], rows, W=12, rungs=FIB, alpha=1.2,
+                                         scale=0.3)
+    assert max_abs(np64(o), o_ref) <= TOL["bf16"]["o"]
+    assert max_abs(np64(lse), lse_ref) <= TOL["bf16"]["lse"]
