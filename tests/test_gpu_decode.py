@@ -109,3 +109,53 @@ def test_decode_explicit_softmax_scale():
                                          scale=0.3)
     assert max_abs(np64(o), o_ref) <= TOL["bf16"]["o"]
     assert max_abs(np64(lse), lse_ref) <= TOL["bf16"]["lse"]
+
+
+def test_decode_bench_shape_from_graph_replay():
+    """The benchmark's launch configuration: 256 sequences over 4096-row
+    caches, the per-layer calls captured once in a CUDA graph on a side stream
+    and replayed; sampled sequences of every layer against the oracle."""
+    from fibonacci_spaced_sparse_gb300 import inputs
+    B, Tc, W, L = 256, 4096, 12, 2
+    alphas = [api.alpha_schedule("linear", 16)[l] for l in (3, 12)]
+    kc = [inputs.normal_on("cuda", (B, Tc, 2, 64), layer=70 + l, stream="k") for l in range(L)]
+    vc = [inputs.normal_on("cuda", (B, Tc, 2, 64), layer=70 + l, stream="v") for l in range(L)]
+    qs = [inputs.normal_on("cuda", (B, 8, 64), layer=70 + l, stream="q") for l in range(L)]
+    rng = np.random.default_rng(70)
+    pos_np = rng.integers(Tc // 2, Tc, B).astype(np.int32)
+    pos_np[:3] = [Tc // 2, Tc - 2, Tc - 1]
+    pos = torch.from_numpy(pos_np).cuda()
+    outs = [torch.empty_like(q) for q in qs]
+    lses = [torch.empty((B, 8), dtype=torch.float32, device="cuda") for _ in range(L)]
+    api.rope_table(Tc, "cuda")
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+
+    def layers(s):
+        for l in range(L):
+            api.sfa_decode(qs[l], kc[l], vc[l], pos, alpha=alphas[l], W=W, out=outs[l], lse=lses[l], stream=s)
+
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        layers(side)
+    main.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        layers(side)
+    for o in outs:
+        o.fill_(float("nan"))
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    for l in range(L):
+        for b in (0, 1, 2, 77, 128, 255):
+            i = int(pos_np[b])
+            q = np.zeros((1, Tc, 8, 64))
+            q[0, i] = qs[l][b].double().cpu().numpy()
+            k = kc[l][b:b + 1].double().cpu().numpy()
+            v = vc[l][b:b + 1].double().cpu().numpy()
+            o_ref, lse_ref = oracle.forward_rows(q, k, v, np.array([[0, i]], dtype=np.int32), W=W,
+                                                 rungs=FIB, alpha=alphas[l])
+            assert max_abs(np64(outs[l][b]), o_ref[0]) <= TOL["bf16"]["o"], (l, b)
+            assert max_abs(np64(lses[l][b]), lse_ref[0]) <= TOL["bf16"]["lse"], (l, b)
