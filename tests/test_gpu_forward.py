@@ -233,3 +233,38 @@ def test_explicit_softmax_scale(dtype, scale, rope):
                                     rope_theta=rope)
     assert max_abs(np64(o), o_ref) <= TOL[dtype]["o"]
     assert max_abs(np64(lse), lse_ref) <= TOL[dtype]["lse"]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_without_lse_output(dtype):
+    """LSE is optional (a NULL pointer): the output is the same as with it."""
+    x, f = draw(2, 150, dtype, layer=64)
+    xd = to_dev(x)
+    o1, _ = gpu_forward(xd, alpha=0.97, W=12, rungs=FIB)
+    o2, l2 = gpu_forward(xd, alpha=0.97, W=12, rungs=FIB, need_lse=False)
+    assert l2 is None
+    assert torch.equal(o1, o2)
+    o_ref, _ = oracle.forward(f["q"], f["k"], f["v"], W=12, rungs=FIB, alpha=0.97)
+    assert max_abs(np64(o2), o_ref) <= TOL[dtype]["o"]
+
+
+def test_layers_and_decode_without_lse_output():
+    """The multi-layer forward and the decode with no LSE output give the same
+    outputs as with it."""
+    xs = [draw(2, 130, "bf16", layer=65 + l)[0] for l in range(3)]
+    xd = [to_dev(x) for x in xs]
+    alphas = [0.8, 1.0, 1.3]
+    a_outs, _ = api.sfa_forward_layers([x["q"] for x in xd], [x["k"] for x in xd], [x["v"] for x in xd],
+                                       alphas=alphas, W=12)
+    b_outs, b_lses = api.sfa_forward_layers([x["q"] for x in xd], [x["k"] for x in xd],
+                                            [x["v"] for x in xd], alphas=alphas, W=12, need_lse=False)
+    torch.cuda.synchronize()
+    assert b_lses is None
+    for a, b in zip(a_outs, b_outs):
+        assert torch.equal(a, b)
+    pos = torch.tensor([0, 129], dtype=torch.int32, device="cuda")
+    q = torch.stack([xd[0]["q"][0, 0], xd[0]["q"][1, 129]])
+    o1, _ = api.sfa_decode(q, xd[0]["k"], xd[0]["v"], pos, alpha=0.8, W=12)
+    o2, l2 = api.sfa_decode(q, xd[0]["k"], xd[0]["v"], pos, alpha=0.8, W=12, need_lse=False)
+    torch.cuda.synchronize()
+    assert l2 is None and torch.equal(o1, o2)
