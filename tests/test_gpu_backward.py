@@ -142,3 +142,27 @@ def test_explicit_softmax_scale_gradients(dtype, scale):
         assert max_abs(np64(got), want) <= bound, name
     terms = float(np.sum(np.asarray(FIB, dtype=np.float64) * np.abs(ref[5])))
     assert abs(float(da.item()) - ref[3]) <= tol["dtheta"] * max(terms, abs(ref[3])) + 1e-6
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_fractional_unsorted_duplicate_base_offsets(dtype):
+    """Any finite positive base offsets: fractional, given out of order, one
+    repeated (the rung plan sorts by distance and keeps repeats as separate
+    entries, as the oracle's key list does)."""
+    rungs = (19.1, 2.5, 7.3, 7.3, 40.25, 13.0)
+    ref = run(2, 140, dtype, alpha=1.11, W=8, rungs=rungs, layer=66)
+    assert np.isfinite(ref[3])
+
+
+def test_fractional_base_offsets_decode():
+    rungs = (19.1, 2.5, 7.3, 7.3, 40.25, 13.0)
+    x, f = draw(4, 120, "bf16", layer=67)
+    pos = np.array([0, 9, 60, 119], dtype=np.int32)
+    qd = torch.stack([x["q"][b, p] for b, p in enumerate(pos)])
+    o, lse = api.sfa_decode(qd.cuda(), x["k"].cuda(), x["v"].cuda(), torch.from_numpy(pos).cuda(),
+                            alpha=1.11, W=8, rungs=rungs)
+    torch.cuda.synchronize()
+    rows = np.stack([np.arange(4, dtype=np.int32), pos], axis=1)
+    o_ref, lse_ref = oracle.forward_rows(f["q"], f["k"], f["v"], rows, W=8, rungs=rungs, alpha=1.11)
+    assert max_abs(np64(o), o_ref) <= TOL["bf16"]["o"]
+    assert max_abs(np64(lse), lse_ref) <= TOL["bf16"]["lse"]
