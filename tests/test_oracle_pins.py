@@ -183,6 +183,18 @@ def test_alpha1_dense_mask_batched(W):
     assert np.max(np.abs(lse - lse_ref)) < 1e-12
 
 
+@pytest.mark.parametrize("scale", [0.05, 0.3])
+def test_explicit_scale_equals_dense_mask_with_that_scale(scale):
+    """A caller-given softmax scale multiplies every score: at alpha = 1 the
+    sparse attention equals masked dense attention at that scale."""
+    x = _inputs(1, 160, layer=5)
+    o, lse = oracle.forward(x["q"], x["k"], x["v"], W=6, rungs=FIB, alpha=1.0, scale=scale)
+    mask = union_mask(160, 6, [f for f in FIB if f > 6])
+    o_ref, lse_ref = sdpa_masked(oracle.rope(x["q"]), oracle.rope(x["k"]), x["v"], mask, scale)
+    assert np.max(np.abs(o - o_ref)) < 1e-12
+    assert np.max(np.abs(lse - lse_ref)) < 1e-12
+
+
 def test_lerp_limit_from_below_is_plain_gather():
     """As alpha -> 1 from below, each rung's fraction t -> 1 and the lerp tends
     to the plain gather of row i - f_k (weight t on the row at distance n + 1)."""
@@ -402,12 +414,15 @@ def test_input_gradients_finite_difference(which):
         assert abs(grad[idx] - fd) <= 1e-7 * max(1.0, abs(fd)), (idx, grad[idx], fd)
 
 
-def test_backward_alpha1_matches_autograd_dense_mask():
+@pytest.mark.parametrize("scale", [1 / 8, 0.3])
+def test_backward_alpha1_matches_autograd_dense_mask(scale):
     """At alpha = 1 the input gradients equal autograd through torch SDPA with
-    the union boolean mask (fp64), with RoPE undone by the chain rule."""
+    the union boolean mask (fp64), with RoPE undone by the chain rule; also at
+    a caller-given softmax scale."""
     T, W = 96, 8
     x = _inputs(1, T, layer=14)
-    dq, dk, dv, _, _, _ = oracle.backward(x["q"], x["k"], x["v"], x["dO"], W=W, rungs=FIB, alpha=1.0)
+    dq, dk, dv, _, _, _ = oracle.backward(x["q"], x["k"], x["v"], x["dO"], W=W, rungs=FIB, alpha=1.0,
+                                          scale=scale)
     mask = torch.from_numpy(union_mask(T, W, [f for f in FIB if f > W]))
     qh = torch.from_numpy(oracle.rope(x["q"])).requires_grad_(True)
     kh = torch.from_numpy(oracle.rope(x["k"])).requires_grad_(True)
@@ -415,7 +430,7 @@ def test_backward_alpha1_matches_autograd_dense_mask():
     q_ = qh.permute(0, 2, 1, 3)
     k_ = kh.permute(0, 2, 1, 3).repeat_interleave(4, dim=1)
     v_ = v.permute(0, 2, 1, 3).repeat_interleave(4, dim=1)
-    o = torch.nn.functional.scaled_dot_product_attention(q_, k_, v_, attn_mask=mask, scale=1 / 8)
+    o = torch.nn.functional.scaled_dot_product_attention(q_, k_, v_, attn_mask=mask, scale=scale)
     (o.permute(0, 2, 1, 3) * torch.from_numpy(x["dO"])).sum().backward()
     dq_ref = oracle.rope(qh.grad.numpy(), inverse=True)
     dk_ref = oracle.rope(kh.grad.numpy(), inverse=True)
