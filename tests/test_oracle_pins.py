@@ -249,6 +249,41 @@ def test_rung_just_outside_window_duplicates_a_window_row():
     assert np.max(np.abs(o - ref.permute(0, 2, 1, 3).numpy())) < 1e-6
 
 
+def test_repeated_rung_is_a_second_entry():
+    """A base offset given twice is two entries of the key list: at alpha = 1
+    (integer distance 13, beyond W = 6) that key's logit carries an extra
+    log(2) in dense attention, from the position where the rung applies."""
+    T, W = 80, 6
+    x = _inputs(1, T, layer=16)
+    o, lse = oracle.forward(x["q"], x["k"], x["v"], W=W, rungs=[13, 13], alpha=1.0)
+    qh, kh = oracle.rope(x["q"]), oracle.rope(x["k"])
+    q = torch.from_numpy(qh).permute(0, 2, 1, 3)
+    k = torch.from_numpy(kh).permute(0, 2, 1, 3).repeat_interleave(4, dim=1)
+    v = torch.from_numpy(x["v"]).permute(0, 2, 1, 3).repeat_interleave(4, dim=1)
+    dd = np.arange(T)[:, None] - np.arange(T)[None, :]
+    bias = np.where(((dd >= 0) & (dd <= W)) | (dd == 13), 0.0, -np.inf)
+    bias = bias + np.where(dd == 13, math.log(2.0), 0.0)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        q, k, v, attn_mask=torch.from_numpy(bias), scale=1 / 8)
+    assert np.max(np.abs(o - ref.permute(0, 2, 1, 3).numpy())) < 1e-12
+
+
+def test_order_of_base_offsets_does_not_matter():
+    """The key list is a set of entries: listing the base offsets in another
+    order changes only the summation order (fractional offsets, alpha != 1)."""
+    x = _inputs(2, 120, layer=17)
+    a = (2.5, 7.3, 13.0, 19.1, 40.25)
+    b = (19.1, 2.5, 40.25, 13.0, 7.3)
+    oa, la = oracle.forward(x["q"], x["k"], x["v"], W=8, rungs=a, alpha=1.11)
+    ob, lb = oracle.forward(x["q"], x["k"], x["v"], W=8, rungs=b, alpha=1.11)
+    assert np.max(np.abs(oa - ob)) < 1e-12 and np.max(np.abs(la - lb)) < 1e-12
+    ga = oracle.backward(x["q"], x["k"], x["v"], x["dO"], W=8, rungs=a, alpha=1.11)
+    gb = oracle.backward(x["q"], x["k"], x["v"], x["dO"], W=8, rungs=b, alpha=1.11)
+    for u, w in zip(ga[:3], gb[:3]):
+        assert np.max(np.abs(u - w)) < 1e-11
+    assert abs(ga[3] - gb[3]) < 1e-9 * max(1.0, abs(ga[3]))
+
+
 def test_integer_rungs_at_alpha_1p5_even_offsets():
     """alpha = 1.5 makes the even offsets integral (3, 12, 51, 216, 915) and the
     odd ones half-integral; with W = 12, every rung is integral or dropped when
