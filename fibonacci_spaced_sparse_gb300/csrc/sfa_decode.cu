@@ -197,10 +197,12 @@ decode_kernel(const LayerArgs a, int Tc, const T* __restrict__ q, const T* __res
 // 16-byte pieces of a row, and the (cos, sin) of those pairs are 64
 // contiguous bytes of the table row, so every load of a cache row is a
 // 16-byte load and all of an entry's rows are in flight together.  A score is
-// the sum of four lanes' partial dot products (two shuffles); the maximum and
-// the sum over the entries go through the warp and a few shared words; the
-// value products of the 32 entries are summed through shared memory (entry
-// stride padded so that the 16-byte writes of a warp hit distinct banks).
+// the sum of four lanes' partial dot products (two shuffles).  Each warp keeps
+// the softmax state of its eight entries (their maximum, the exponentials and
+// their sum against it); the value products of the 32 entries go through
+// shared memory (entry stride padded so that the 16-byte writes of a warp hit
+// distinct banks), and one block barrier later every output is each warp's
+// sum merged with the weights 2^(m_warp - m) of the four warps' maxima.
 constexpr int kFastEntries = 32;
 constexpr int kFastThreads = 128;
 constexpr int kRedStride = 4 * kD + 4;  // floats per entry in the value-product buffer
@@ -344,29 +346,25 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
         acc += __shfl_xor_sync(kFull, acc, 2);
         s[h] = live ? acc * sl2 : -INFINITY;
     }
-    // the maximum over the key list (entry 0, the query's own row, is always live)
-    float mx[kG];
-#pragma unroll
-    for (int h = 0; h < kG; ++h) {
-        mx[h] = s[h];
-#pragma unroll
-        for (int w = 4; w <= 16; w <<= 1) mx[h] = fmaxf(mx[h], __shfl_xor_sync(kFull, mx[h], w));
-    }
-    if (lane == 0) {
-#pragma unroll
-        for (int h = 0; h < kG; ++h) mw[warp][h] = mx[h];
-    }
-    __syncthreads();
+    // softmax state per warp (its eight entries): the warp's maximum, and the
+    // exponentials and their sum against it; the four warps' states are
+    // merged at the end (a warp whose entries are all past the list has
+    // maximum -inf and weight 0; warp 0 holds entry 0, the query's own row,
+    // which is always live)
     float p[kG];
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
-        const float M = fmaxf(fmaxf(mw[0][h], mw[1][h]), fmaxf(mw[2][h], mw[3][h]));
-        p[h] = live ? exp2f(s[h] - M) : 0.f;
+        float m = s[h];
+#pragma unroll
+        for (int w = 4; w <= 16; w <<= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, w));
+        p[h] = live ? exp2f(s[h] - m) : 0.f;
         float l = p[h];
 #pragma unroll
         for (int w = 4; w <= 16; w <<= 1) l += __shfl_xor_sync(kFull, l, w);
-        if (lane == 0) lw[warp][h] = l;
-        mx[h] = M;
+        if (lane == 0) {
+            mw[warp][h] = m;
+            lw[warp][h] = l;
+        }
     }
     // p v of this entry, chunk c, into the reduction buffer
     float* rr = red + e * kRedStride;
@@ -380,23 +378,29 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
         dy[1] = make_float4(p[h] * vv[12], p[h] * vv[13], p[h] * vv[14], p[h] * vv[15]);
     }
     __syncthreads();
-    // thread (h, d): outputs d and d + 32 of head h, summed over the entries in order
+    // thread (h, d): outputs d and d + 32 of head h -- each warp's entries
+    // summed in order, the four sums merged with weights 2^(m_w - M)
     {
         const int h = tid >> 5, d = tid & 31;
-        float o0 = 0.f, o1 = 0.f;
-#pragma unroll 8
-        for (int en = 0; en < kFastEntries; ++en) {
-            o0 += red[en * kRedStride + h * kD + d];
-            o1 += red[en * kRedStride + h * kD + kPairs + d];
+        const float M = fmaxf(fmaxf(mw[0][h], mw[1][h]), fmaxf(mw[2][h], mw[3][h]));
+        float o0 = 0.f, o1 = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float cw = mw[w][h] == -INFINITY ? 0.f : exp2f(mw[w][h] - M);
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int en = 8 * w; en < 8 * w + 8; ++en) {
+                a0 += red[en * kRedStride + h * kD + d];
+                a1 += red[en * kRedStride + h * kD + kPairs + d];
+            }
+            o0 = fmaf(cw, a0, o0);
+            o1 = fmaf(cw, a1, o1);
+            L = fmaf(cw, lw[w][h], L);
         }
-        const float L = (lw[0][h] + lw[1][h]) + (lw[2][h] + lw[3][h]);
         const float inv = 1.f / L;
         o[qbase + h * kD + d] = __float2bfloat16_rn(o0 * inv);
         o[qbase + h * kD + kPairs + d] = __float2bfloat16_rn(o1 * inv);
-        if (lse && d == 0) {
-            const float M = fmaxf(fmaxf(mw[0][h], mw[1][h]), fmaxf(mw[2][h], mw[3][h]));
-            lse[(size_t)b * kHq + g * kG + h] = (M + log2f(L)) * kLn2;
-        }
+        if (lse && d == 0) lse[(size_t)b * kHq + g * kG + h] = (M + log2f(L)) * kLn2;
     }
 }
 
