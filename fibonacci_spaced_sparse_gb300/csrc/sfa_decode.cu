@@ -201,8 +201,9 @@ decode_kernel(const LayerArgs a, int Tc, const T* __restrict__ q, const T* __res
 // the softmax state of its eight entries (their maximum, the exponentials and
 // their sum against it); the value products of the 32 entries go through
 // shared memory (entry stride padded so that the 16-byte writes of a warp hit
-// distinct banks), and one block barrier later every output is each warp's
-// sum merged with the weights 2^(m_warp - m) of the four warps' maxima.
+// distinct banks), and after the one block barrier every output is each
+// warp's sum merged with the weights 2^(m_warp - m) of the four warps'
+// maxima.  Each lane rotates the query chunk it scores with itself.
 constexpr int kFastEntries = 32;
 constexpr int kFastThreads = 128;
 constexpr int kRedStride = 4 * kD + 4;  // floats per entry in the value-product buffer
@@ -261,16 +262,21 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
     const LayerArgs a, int Tc, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ pos, const float2* __restrict__ rope,
     __nv_bfloat16* __restrict__ o, float* __restrict__ lse, unsigned* __restrict__ status) {
-    __shared__ __align__(16) float qh[kG][kD];                   // the rotated query, fp32
     __shared__ __align__(16) float red[kFastEntries * kRedStride];  // p v per entry
     __shared__ float mw[4][kG], lw[4][kG];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = blockIdx.x % kHkv, b = blockIdx.x / kHkv;
     const size_t qbase = ((size_t)b * kHq + g * kG) * kD;
-    // thread (h, m) rotates pair m of head h of the query; its two values are
-    // loaded together with the position
-    const int qh_h = tid >> 5, qh_m = tid & 31;
-    const __nv_bfloat16 qx_raw = q[qbase + qh_h * kD + qh_m], qy_raw = q[qbase + qh_h * kD + kPairs + qh_m];
+    const int c = lane & 3, e = warp * 8 + (lane >> 2);
+    // the query's chunk c of every head (dimensions 8c .. 8c + 7 and their
+    // partners), loaded together with the position; each lane rotates the
+    // chunk it scores with itself, so no shared copy and no barrier is needed
+    uint4 qxw[kG], qyw[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+        qxw[h] = __ldg(reinterpret_cast<const uint4*>(q + qbase + h * kD) + c);
+        qyw[h] = __ldg(reinterpret_cast<const uint4*>(q + qbase + h * kD) + 4 + c);
+    }
     const int i = __ldg(pos + b);
     if (i < 0 || i >= Tc) {
         // a position outside the cache: report it, read nothing, output zeros
@@ -282,7 +288,6 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
     }
     // this lane's entry: window distances 0..min(W, i), then the rungs with
     // ceil(d) <= i (a prefix of the kept list, which is sorted by distance)
-    const int c = lane & 3, e = warp * 8 + (lane >> 2);
     const int nwin = min(a.W, i) + 1;
     int nact = 0;
     for (int r = 0; r < a.nr; ++r) nact += (a.r[r].c <= i) ? 1 : 0;
@@ -309,11 +314,14 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
         const size_t off = (((size_t)b * Tc + rb) * kHkv + g) * kD;
         fetch_row(kc + off, vc + off, rope, rb, c, Bw);
     }
-    {
-        const float x = __bfloat162float(qx_raw), y = __bfloat162float(qy_raw);
-        const float2 cs = rope_cs(rope, i, qh_m);
-        qh[qh_h][qh_m] = x * cs.x - y * cs.y;
-        qh[qh_h][kPairs + qh_m] = y * cs.x + x * cs.y;
+    float4 qcs[4];
+    if (rope) {
+        const float4* t = reinterpret_cast<const float4*>(rope + (size_t)i * kPairs + 8 * c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qcs[j] = __ldg(t + j);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) qcs[j] = make_float4(1.f, 0.f, 1.f, 0.f);
     }
     float kx[8], ky[8], vv[16];
     unpack_row(A, kx, ky, vv);
@@ -328,19 +336,20 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
 #pragma unroll
         for (int j = 0; j < 16; ++j) vv[j] = wa * vv[j] + wb * bv[j];
     }
-    __syncthreads();  // qh
     const float sl2 = a.scale * kLog2e;
     float s[kG];
 #pragma unroll
     for (int h = 0; h < kG; ++h) {
-        const float4* qx = reinterpret_cast<const float4*>(&qh[h][8 * c]);
-        const float4* qy = reinterpret_cast<const float4*>(&qh[h][kPairs + 8 * c]);
+        const uint32_t xw[4] = {qxw[h].x, qxw[h].y, qxw[h].z, qxw[h].w};
+        const uint32_t yw[4] = {qyw[h].x, qyw[h].y, qyw[h].z, qyw[h].w};
         float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const float4 u = qx[j], w = qy[j];
-            acc += u.x * kx[4 * j] + u.y * kx[4 * j + 1] + u.z * kx[4 * j + 2] + u.w * kx[4 * j + 3];
-            acc += w.x * ky[4 * j] + w.y * ky[4 * j + 1] + w.z * ky[4 * j + 2] + w.w * ky[4 * j + 3];
+        for (int j = 0; j < 4; ++j) {
+            // pairs 2j, 2j + 1 of the chunk, rotated at the query's position
+            const float2 x = bf2(xw[j]), y = bf2(yw[j]);
+            const float qx0 = x.x * qcs[j].x - y.x * qcs[j].y, qy0 = y.x * qcs[j].x + x.x * qcs[j].y;
+            const float qx1 = x.y * qcs[j].z - y.y * qcs[j].w, qy1 = y.y * qcs[j].z + x.y * qcs[j].w;
+            acc += qx0 * kx[2 * j] + qx1 * kx[2 * j + 1] + qy0 * ky[2 * j] + qy1 * ky[2 * j + 1];
         }
         acc += __shfl_xor_sync(kFull, acc, 1);
         acc += __shfl_xor_sync(kFull, acc, 2);
