@@ -38,6 +38,7 @@ UNIT = "query-tokens/s"
 IDEAL_BYTES_PER_TOKEN = 2 * (8 * 64 + 2 * 64 + 2 * 64 + 8 * 64)  # bf16 Q, K, V read + O write
 FALLBACK_HBM_GBS = 6800.0
 E2E_MAX_STEPS = 20
+SOAK_S = 1.0  # untimed run of the step right before the timed region (clock samples)
 REFERENCE_BUDGET_S = 90.0  # oracle time of a whole --impl reference run
 
 
@@ -52,6 +53,7 @@ def parse():
                              "decode", "front-end"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-backward", action="store_true")
     return ap.parse_args()
 
 
@@ -133,11 +135,12 @@ def measured_peak():
 # ------------------------------------------------------------------ clocks --
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 50
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -147,7 +150,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.INTERVAL_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
@@ -223,6 +226,38 @@ def recorded_traffic(workload_name):
 
 # ----------------------------------------------------------- CPU baseline --
 
+def oracle_alphas(wl):
+    """The workload's per-layer alphas as the oracle states the schedules (the
+    CPU arms never load the CUDA library)."""
+    from oracle import oracle
+    from fibonacci_spaced_sparse_gb300 import inputs
+    if wl.schedule == "learned":
+        return oracle.schedule_learned(inputs.thetas(wl.layers, wl.theta_sigma, seed=42))
+    if wl.schedule == "linear":
+        return oracle.schedule_linear(wl.layers)
+    if wl.schedule == "coprime":
+        return oracle.schedule_coprime(wl.layers, 7)
+    return oracle.schedule_fixed(wl.layers)
+
+
+def oracle_rungs(wl):
+    """The workload's base offsets from the oracle's own tables."""
+    from oracle import oracle
+    return oracle.FIBONACCI_BASE if wl.base == "fibonacci" else oracle.pow2_base(wl.T)
+
+
+def config_of(wl, world):
+    """The ``config`` object of a bench line (the same for both arms)."""
+    L = wl.layers
+    return {"workload": wl.name, "B": wl.B, "T": wl.T, "W": list(wl.W),
+            "layers": L, "schedule": wl.schedule, "base": wl.base,
+            "heads": "8q/2kv", "head_dim": 64,
+            "backward": wl.backward,
+            "l2": f"inputs larger than L2 ({L * 50.3 * wl.tokens / 32768:.0f} MB of "
+                  "Q/K/V per step), no flush",
+            "parallelism": f"replicas x{world}"}
+
+
 def host_cpu() -> str:
     """The host CPU as /proc/cpuinfo names it (model name on x86; implementer
     and part number on Arm, e.g. 0x41/0xd4f for a Neoverse V2 / Grace core)."""
@@ -252,7 +287,7 @@ def cpu_baseline(wl, budget_s=12.0):
     from fibonacci_spaced_sparse_gb300 import inputs
     from oracle import oracle
     oracle.build()
-    alphas, _ = wl.alphas()
+    alphas, rungs = oracle_alphas(wl), oracle_rungs(wl)
     cores = oracle.default_threads()
     data = {}
     tokens, spent, calls = 0, 0.0, 0
@@ -264,7 +299,7 @@ def cpu_baseline(wl, budget_s=12.0):
             data[l] = {k: v.to(torch.float64).numpy() for k, v in x.items()}
         f = data[l]
         t0 = time.perf_counter()
-        oracle.forward(f["q"], f["k"], f["v"], W=wl.window(l), rungs=wl.rungs(), alpha=alphas[l],
+        oracle.forward(f["q"], f["k"], f["v"], W=wl.window(l), rungs=rungs, alpha=alphas[l],
                        nthreads=cores)
         spent += time.perf_counter() - t0
         tokens += wl.B * wl.T
@@ -323,17 +358,24 @@ def run_ours(args, rank, world, local):
 
     use_dist = init_dist(world, dev)
 
+    t_warm = time.perf_counter()
     for _ in range(max(3, args.warmup)):
         step()
     barrier(dev)
+    step_s = (time.perf_counter() - t_warm) / max(3, args.warmup)
 
     # device-timed region: K steps, per-launch events on the launching stream
     nev = 2 + (2 * L if wl.backward else 0)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nev)] for _ in range(args.steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n0 = api.launch_count()
+    n0 = -1
     with ClockSampler(local) as clk:
+        # the same step, untimed, for about SOAK_S seconds right before the
+        # timed region, so that the clock record has enough samples under this
+        # load even when K steps take only milliseconds
+        soak(step, step_s, dev)
         barrier(dev)
+        n0 = api.launch_count()
         start.record(stream)
         for s in range(args.steps):
             step(ev[s])
@@ -363,7 +405,10 @@ def run_ours(args, rank, world, local):
     if rank == 0 and not args.no_cpu and world == 1:
         cpu = cpu_baseline(wl)
 
-    if wl.backward:
+    if args.workload == "model-shape" and not args.no_backward:
+        # the training step's backward, timed beside the headline forward
+        backward = time_backward(dev, stream, rank)
+    elif wl.backward:
         bwd_avg = statistics.mean(bwd_ms) / 1e3
         # backward ideal bytes: read Q, K, V, O, dO and write dQ, dK, dV once (bf16)
         bwd_ideal = 2 * (8 * 64 + 2 * 64 + 2 * 64 + 8 * 64 + 8 * 64 + 8 * 64 + 2 * 64 + 2 * 64) * wl.B * wl.T
@@ -372,19 +417,17 @@ def run_ours(args, rank, world, local):
                     "frac": bwd_ideal / bwd_avg / 1e9 / peak}
     else:
         backward = None
+    clocks = clk.summary()
+    if clocks:
+        clocks["window"] = f"{SOAK_S:.1f} s of the same step untimed, then the timed region"
+        clocks["ms_per_step_x_sm_mhz"] = elapsed_ms / args.steps * clocks["sm_mhz"]
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
             "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "W": list(wl.W),
-                       "layers": L, "schedule": wl.schedule, "base": wl.base,
-                       "heads": "8q/2kv", "head_dim": 64,
-                       "backward": wl.backward,
-                       "l2": f"inputs larger than L2 ({L * 50.3 * wl.tokens / 32768:.0f} MB of "
-                             "Q/K/V per step), no flush",
-                       "parallelism": f"replicas x{world}"},
+            "config": config_of(wl, world),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "kernel": "forward attention (fwd_mma_kernel)",
@@ -398,12 +441,74 @@ def run_ours(args, rank, world, local):
             "backward": backward,
             "e2e": e2e,
             "gpu_launches": launches,
-            "clocks": clk.summary(),
+            "clocks": clocks,
         }
         print(json.dumps(line), flush=True)
     if use_dist:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def soak(step, step_s, dev):
+    """Runs ``step`` untimed for about SOAK_S seconds (at least one step)."""
+    import torch
+    n = max(1, int(SOAK_S / max(step_s, 1e-4)))
+    for _ in range(n):
+        step()
+    torch.cuda.synchronize(dev)
+
+
+def time_backward(dev, stream, rank, layers=4, iters=10):
+    """The backward of the training-step workload (B=32, T=1024, W=12,
+    Fibonacci base, learned-style alpha = 0.5 + sigmoid(theta), theta ~ N(0,
+    0.5)), timed layer by layer with CUDA events on the launching stream after
+    a forward of each layer: the per-layer time and its fraction of HBM peak
+    on the ideal bytes (one read of Q, K, V, O, dO and one write of dQ, dK,
+    dV).  ``layers`` of the 16 layers, each its own seeded inputs."""
+    import torch
+    from fibonacci_spaced_sparse_gb300 import api, inputs
+    wl = workload_of("train-step")
+    alphas, _ = wl.alphas()
+    W, rungs = wl.window(0), wl.rungs()
+    d = [{k: v.to(dev) for k, v in inputs.qkv(wl.B, wl.T, dtype=torch.bfloat16, seed=replica_seed(rank),
+                                              layer=l, with_dO=True).items()} for l in range(layers)]
+    outs, lses = [], []
+    for l in range(layers):
+        o, lse = api.sfa_forward(d[l]["q"], d[l]["k"], d[l]["v"], alpha=alphas[l], W=W, rungs=rungs)
+        outs.append(o)
+        lses.append(lse)
+    need = max(api.sfa_backward_workspace_size(wl.B, wl.T, alpha=alphas[l], W=W, rungs=rungs)
+               for l in range(layers))
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    grads = [(torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"]),
+              torch.empty(1, dtype=torch.float32, device=dev), torch.empty(1, dtype=torch.float32, device=dev))
+             for x in d]
+
+    def one(l):
+        api.sfa_backward(d[l]["q"], d[l]["k"], d[l]["v"], outs[l], d[l]["dO"], lses[l], alpha=alphas[l],
+                         W=W, rungs=rungs, workspace=ws, out=grads[l])
+
+    for _ in range(3):
+        for l in range(layers):
+            one(l)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters * layers)]
+    for it in range(iters):
+        for l in range(layers):
+            a, b = ev[it * layers + l]
+            a.record(stream)
+            one(l)
+            b.record(stream)
+    torch.cuda.synchronize(dev)
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1e3
+    ideal = 2 * (8 * 64 * 4 + 2 * 64 * 4) * wl.B * wl.T
+    peak, peak_kind = measured_peak()
+    return {"workload": wl.name + " (backward only)", "layers_timed": layers, "calls": iters * layers,
+            "avg_launch_us": us, "ideal_bytes_per_call": ideal, "achieved": ideal / (us * 1e-6) / 1e9,
+            "peak": peak, "unit": "GB/s", "frac": ideal / (us * 1e-6) / 1e9 / peak, "peak_kind": peak_kind,
+            "note": "per-layer sfa_backward call (all its launches), CUDA events on the launching stream, "
+                    "inputs larger than L2"}
 
 
 def run_e2e(args, wl, alphas, host, dev, stream, world, use_dist):
@@ -697,7 +802,7 @@ def run_reference(args, rank, world):
     from oracle import oracle
     oracle.build()
     wl = workload_of(args.workload)
-    alphas, _ = wl.alphas()
+    alphas, rungs = oracle_alphas(wl), oracle_rungs(wl)
     cores = oracle.default_threads()
     nl = min(wl.layers, 4)
     data = []
@@ -708,7 +813,7 @@ def run_reference(args, rank, world):
     def run(l, b0, n):
         f = data[l]
         oracle.forward(f["q"][b0:b0 + n], f["k"][b0:b0 + n], f["v"][b0:b0 + n], W=wl.window(l),
-                       rungs=wl.rungs(), alpha=alphas[l], nthreads=cores)
+                       rungs=rungs, alpha=alphas[l], nthreads=cores)
 
     t0 = time.perf_counter()
     run(0, 0, 1)
@@ -731,8 +836,7 @@ def run_reference(args, rank, world):
         "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "W": list(wl.W),
-                   "layers": wl.layers, "schedule": wl.schedule, "base": wl.base},
+        "config": config_of(wl, world),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "cpu": host_cpu(), "sample": f"{n_seq} of {wl.B} sequences ({n_seq * wl.T} query tokens) of one "
                                    f"layer per step, layers 0..{nl - 1} in turn, sized for about "

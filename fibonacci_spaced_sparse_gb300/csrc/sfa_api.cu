@@ -11,6 +11,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <cuda.h>
+
 #include "sfa.h"
 #include "sfa_internal.cuh"
 
@@ -18,6 +20,36 @@ namespace sfa {
 
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+void* driver_entry(const char* name, int version) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return fn;
+}
+
+}  // namespace
+
+// The driver's context id (cuCtxGetId, unique for the life of the process),
+// plus one so that a valid id never reads as "no context".
+unsigned long long context_key() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static const GetCurrent get_current = reinterpret_cast<GetCurrent>(driver_entry("cuCtxGetCurrent", 4000));
+    static const GetId get_id = reinterpret_cast<GetId>(driver_entry("cuCtxGetId", 12000));
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id + 1;
+}
 
 // Test hook: SFA_TEST_FAULT=launch in the environment (read once) makes every
 // entry point fail with SFA_ERR_CUDA after its argument checks, before it

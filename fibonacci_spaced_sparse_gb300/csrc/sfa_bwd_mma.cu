@@ -241,8 +241,8 @@ __device__ __forceinline__ void start_bunit(const BwdParams& P, const Smem& S, c
                 const int m = 16 * s + 8 * h + 2 * tig;
                 const float4 cs = lds_f4(trow + (uint32_t)(m * 8));
                 const float2 xv = unpack_bf16(U.qf[s][h]), yv = unpack_bf16(U.qf[s + 2][h]);
-                U.qf[s][h] = pack_bf16(xv.x * cs.x - yv.x * cs.y, xv.y * cs.z - yv.y * cs.w);
-                U.qf[s + 2][h] = pack_bf16(yv.x * cs.x + xv.x * cs.y, yv.y * cs.z + xv.y * cs.w);
+                U.qf[s][h] = rope_x(xv, yv, cs);
+                U.qf[s + 2][h] = rope_y(xv, yv, cs);
             }
     }
 #pragma unroll
@@ -666,8 +666,8 @@ __global__ void __launch_bounds__(kPrepThreads) bwd_prep_kernel(const __nv_bfloa
         const float4 t = __ldg(cs + c);
         const float2 x = unpack_bf16(u4_get(xv, c));
         const float2 y = unpack_bf16(u4_get(yv, c));
-        xo[c] = pack_bf16(x.x * t.x - y.x * t.y, x.y * t.z - y.y * t.w);
-        yo[c] = pack_bf16(y.x * t.x + x.x * t.y, y.y * t.z + x.y * t.w);
+        xo[c] = rope_x(x, y, t);
+        yo[c] = rope_y(x, y, t);
     }
     __nv_bfloat16* out = khat + (size_t)row * kD;
     *reinterpret_cast<uint4*>(out + 8 * a) = make_uint4(xo[0], xo[1], xo[2], xo[3]);
@@ -838,11 +838,11 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     }
     const size_t smem = 1024 + kHeaderBytes + BwdParams::kQMaps * (size_t)kQTileBytes + (size_t)P.win_slot_bytes +
                         NGS * (size_t)kGroupSlotBytes + NCW * (size_t)kObufBytes + kDtBytes + 1024 + NCW * 8192;
-    static size_t configured_smem[64];
-    if (configured_smem[dev & 63] < smem) {
+    static CtxSetting configured_smem[64];
+    if (!ctx_setting_holds(configured_smem[dev & 63], smem)) {
         e = cudaFuncSetAttribute(bwd_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured_smem[dev & 63] = smem;
+        ctx_setting_done(configured_smem[dev & 63], smem);
     }
     // CTAs per SM for this shared-memory size (looked up once per device and
     // size, so that no runtime query runs while a stream is being captured)

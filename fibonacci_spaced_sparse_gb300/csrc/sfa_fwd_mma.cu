@@ -201,8 +201,8 @@ __device__ __forceinline__ void start_unit(const FwdParams& P, const Smem& S, in
             const float4 cs = lds_f4(trow + (uint32_t)(w * 16));
             const float2 xv = unpack_bf16(u4_get(x4, w));
             const float2 yv = unpack_bf16(u4_get(y4, w));
-            U.qf[w >> 1][w & 1] = pack_bf16(xv.x * cs.x - yv.x * cs.y, xv.y * cs.z - yv.y * cs.w);
-            U.qf[2 + (w >> 1)][w & 1] = pack_bf16(yv.x * cs.x + xv.x * cs.y, yv.y * cs.z + xv.y * cs.w);
+            U.qf[w >> 1][w & 1] = rope_x(xv, yv, cs);
+            U.qf[2 + (w >> 1)][w & 1] = rope_y(xv, yv, cs);
         }
     } else {
 #pragma unroll
@@ -710,7 +710,7 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
     if (e != cudaSuccess) return e;
     const int sms = sm_count(dev, &e);
     if (e != cudaSuccess) return e;
-    static size_t configured_smem[2][64];  // per variant and device: dynamic shared memory already allowed
+    static CtxSetting configured_smem[2][64];  // per variant and device: dynamic shared memory already allowed
     FwdParams P;
     std::memset(&P, 0, sizeof(P));
     P.a = a;
@@ -745,12 +745,12 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
     const int kidx = integer_offsets ? 1 : 0;
     const size_t smem = 1024 + kHeaderBytes + FwdParams::kQMaps * (size_t)kQTileBytes + (size_t)P.win_slot_bytes +
                         NGS * (size_t)kGroupSlotBytes + NCW * (size_t)kObufBytes;
-    if (configured_smem[kidx][dev & 63] < smem) {
+    if (!ctx_setting_holds(configured_smem[kidx][dev & 63], smem)) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
-        configured_smem[kidx][dev & 63] = smem;
+        ctx_setting_done(configured_smem[kidx][dev & 63], smem);
     }
     // CTAs per SM for this shared-memory size (looked up once per device and
     // size, so that no runtime query runs while a stream is being captured)

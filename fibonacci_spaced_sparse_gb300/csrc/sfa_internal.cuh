@@ -41,6 +41,32 @@ struct LayerArgs {
 
 // Host: count of kernel launches made by the library.
 void count_launch();
+
+// Host: a key of the CUDA context current on the calling thread, unique for
+// the life of the process (a context created after another one was destroyed,
+// or by a device reset, never gets the old key); 0 when no context is current
+// or the driver cannot say.  Set-up that lives in a context (kernel attributes,
+// device addresses of library symbols) is recorded with this key and redone
+// when the key differs.
+unsigned long long context_key();
+
+// Host: set-up of one kernel attribute value done in one context, per device.
+struct CtxSetting {
+    unsigned long long key;  // context_key() when it was done (0: never)
+    size_t value;
+};
+
+// True when `s` records `value` or more, set in the context current now.
+inline bool ctx_setting_holds(const CtxSetting& s, size_t value) {
+    const unsigned long long k = context_key();
+    return k != 0 && s.key == k && s.value >= value;
+}
+
+inline void ctx_setting_done(CtxSetting& s, size_t value) {
+    s.value = value;
+    s.key = context_key();
+}
+
 // SFA_TEST_FAULT=launch in the environment: entry points fail with
 // SFA_ERR_CUDA after their argument checks, before they launch anything.
 bool fault_injected();

@@ -10,8 +10,11 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds its 8 MiB until the process exits.  In host code its name is
-// only a host-side handle, so the device address is looked up once per device
-// with cudaGetSymbolAddress (with that device current) and cached here.
+// only a host-side handle.  Its device address belongs to one CUDA context:
+// it is looked up with cudaGetSymbolAddress in the context current at the
+// call and cached under that context's key (sfa::context_key), so a caller
+// that switches to a context of its own (cuCtxCreate) gets the address that
+// is valid in the context it calls from.
 #include <mutex>
 
 #include "sfa.h"
@@ -24,10 +27,14 @@ constexpr size_t kScratchBytes = size_t(8) << 20;  // 8 MiB
 __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices];
+struct ScratchAddr {
+    unsigned long long key;  // context the address was looked up in (0: none yet)
+    void* addr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
 
-// Device address of g_scratch on the current device (looked up on first use).
+// Device address of g_scratch in the context current on this thread.
 sfa_status scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -36,15 +43,19 @@ sfa_status scratch_address(void** out) {
     }
     if (dev < 0 || dev >= kMaxDevices) return SFA_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    ScratchAddr& slot = g_scratch_addr[dev];
+    const unsigned long long key = sfa::context_key();
+    if (key == 0 || slot.key != key) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || !p) {
             (void)cudaGetLastError();
             return SFA_ERR_CUDA;
         }
-        g_scratch_addr[dev] = p;
+        // the lookup makes the runtime's context current if none was
+        slot.key = sfa::context_key();
+        slot.addr = p;
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return SFA_OK;
 }
 

@@ -413,11 +413,11 @@ cudaError_t launch_qkv_rope(int M, int T, int dm, const void* x, const void* w, 
     if (e != cudaSuccess) return e;
     const int sms = ring::sm_count(dev, &e);
     if (e != cudaSuccess) return e;
-    static bool configured[64];
-    if (!configured[dev & 63]) {
+    static CtxSetting configured[64];
+    if (!ctx_setting_holds(configured[dev & 63], kSmemBytes)) {
         e = cudaFuncSetAttribute(qkv_rope_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        configured[dev & 63] = true;
+        ctx_setting_done(configured[dev & 63], kSmemBytes);
     }
     const int grid = P.tiles < sms ? P.tiles : sms;
     qkv_rope_kernel<<<grid, kThreads, kSmemBytes, s>>>(P);

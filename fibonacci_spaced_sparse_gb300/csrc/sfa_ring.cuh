@@ -267,8 +267,10 @@ __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
 
 // RoPE of two rotation pairs held as bf16 pairs x = (x_m, x_m+1) (dimensions
 // m, m + 1) and y (their partners + D/2), c = (cos_m, sin_m, cos_m+1,
-// sin_m+1): the rotated x and y halves, packed to bf16.  Explicit roundings,
-// so that every kernel that rotates keys produces the same bits.
+// sin_m+1): the rotated x and y halves, packed to bf16.  Explicit roundings
+// (the product rounded to fp32, one fused multiply-add, round to nearest
+// bf16), so that every kernel that rotates queries or keys produces the same
+// bits.
 __device__ __forceinline__ uint32_t rope_x(float2 x, float2 y, float4 c) {
     return pack_bf16(__fmaf_rn(x.x, c.x, __fmul_rn(-y.x, c.y)), __fmaf_rn(x.y, c.z, __fmul_rn(-y.y, c.w)));
 }

@@ -223,9 +223,13 @@ SFA_API sfa_status sfa_forward_layers(const sfa_params *p, int L, const float *a
  * GPU that loads the library holds until the process exits.
  *   - Returns SFA_ERR_UNSUPPORTED, before any launch, when the shape needs
  *     more scratch than that; other errors as sfa_forward.
- *   - Allocates nothing.  The first call on a device looks the array's device
- *     address up (cudaGetSymbolAddress, with that device current) and caches
- *     it; make that first call on each device before any stream capture.
+ *   - Allocates nothing.  The first call in each CUDA context (a device's
+ *     primary context, or one the caller created with cuCtxCreate and made
+ *     current) looks the array's device address up with cudaGetSymbolAddress
+ *     in that context and caches it under the context's id (cuCtxGetId, never
+ *     reused within a process), so every call uses the address valid in the
+ *     context it is made from.  Make the first call in each context before
+ *     any stream capture.
  *   - All calls share the one array: calls that overlap on the GPU (other
  *     streams, other threads) race on it and give wrong results; order them
  *     on one stream.  Nothing in the array needs to start at zero. */

@@ -7,7 +7,7 @@ import torch
 
 from fibonacci_spaced_sparse_gb300 import api, inputs, workloads
 from oracle import oracle
-from _helpers import TOL, draw, max_abs, np64, to_dev
+from _helpers import TOL, cancellation_limit, check_dalpha_dtheta, kernel_rotation, draw, max_abs, np64, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -29,10 +29,7 @@ def run(B, T, dtype, *, alpha, W, rungs=FIB, layer=0, rope_theta=1e4):
         err = max_abs(np64(got), want)
         bound = tol["grad"] * max(1.0, float(np.abs(want).max()) if want.size else 1.0)
         assert err <= bound, (name, err, bound)
-    da_ref, dth_ref = ref[3], ref[4]
-    assert abs(float(dth.item()) - dth_ref) <= tol["dtheta"] * max(abs(dth_ref), 1e-3), (
-        float(dth.item()), dth_ref)
-    assert abs(float(da.item()) - da_ref) <= tol["dtheta"] * max(abs(da_ref), 1e-3)
+    check_dalpha_dtheta(float(da.item()), float(dth.item()), ref[3], ref[4], dtype)
     return ref
 
 
@@ -101,47 +98,59 @@ def test_bf16_without_rope_and_many_rungs():
     run(1, 240, "bf16", alpha=1.07, W=8, rungs=rungs, layer=9)
 
 
-@pytest.mark.parametrize("dtype,rope", [("bf16", 0.0), ("f32", 1e4)])
+def _oracle_grads(x, f, dtype, rope, **kw):
+    """(dq, dk, dv, dalpha, dtheta) of the fp64 oracle for the kernels'
+    inputs.  bf16 with RoPE: the oracle differentiates at the rows the kernels
+    score (the bf16-rounded rotation of kernel_rotation) with its own rotation
+    off, and its gradients with respect to those rotated rows are turned back
+    into gradients of Q and K by the inverse rotation, in fp64."""
+    if dtype == "bf16" and rope > 0:
+        qr, kr = kernel_rotation(x["q"], rope), kernel_rotation(x["k"], rope)
+        ref = oracle.backward(qr.double().numpy(), kr.double().numpy(), f["v"], f["dO"], rope_theta=0.0, **kw)
+        return (oracle.rope(ref[0], rope, inverse=True), oracle.rope(ref[1], rope, inverse=True), ref[2],
+                ref[3], ref[4], ref[5])
+    return oracle.backward(f["q"], f["k"], f["v"], f["dO"], rope_theta=rope, **kw)
+
+
+def _check_grads(got, ref, dtype, rungs=FIB):
+    tol = TOL[dtype]
+    for name, g, want in zip(("dq", "dk", "dv"), got[:3], ref[:3]):
+        bound = tol["grad"] * max(1.0, float(np.abs(want).max()))
+        err = max_abs(np64(g), want)
+        assert err <= bound, (name, err, bound)
+    check_dalpha_dtheta(float(got[3].item()), float(got[4].item()), ref[3], ref[4], dtype,
+                        known_limit=cancellation_limit(rungs, ref[5], ref[3], dtype))
+
+
+@pytest.mark.parametrize("dtype,rope", [("bf16", 0.0), ("bf16", 1e4), ("f32", 1e4)])
 def test_sharp_softmax_gradients(dtype, rope):
     """Q and K scaled by 6 (scores spread over about 50 log2 units): the
     recomputed probabilities exp(s - LSE) are close to 0 or 1 and dS is large.
-    bf16 without RoPE, so that both sides score the identical bf16 bytes."""
+    bf16 with RoPE against the oracle at the kernels' rounded rotation (see
+    _oracle_grads)."""
     x, _ = draw(2, 300, dtype, layer=32, with_dO=True)
     for n in ("q", "k"):
         x[n] = (x[n].float() * 6.0).to(x[n].dtype)
     f = {n: v.to(torch.float64).numpy() for n, v in x.items()}
     xd = to_dev(x)
-    kw = dict(alpha=1.21, W=12, rungs=FIB, rope_theta=rope)
-    o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], **kw)
-    dq, dk, dv, da, dth = api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse, **kw)
+    kw = dict(alpha=1.21, W=12, rungs=FIB)
+    o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], rope_theta=rope, **kw)
+    got = api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse, rope_theta=rope, **kw)
     torch.cuda.synchronize()
-    ref = oracle.backward(f["q"], f["k"], f["v"], f["dO"], W=12, rungs=FIB, alpha=1.21, rope_theta=rope)
-    tol = TOL[dtype]
-    for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
-        err = max_abs(np64(got), want)
-        bound = tol["grad"] * max(1.0, float(np.abs(want).max()))
-        assert err <= bound, (name, err, bound)
-    # dL/dalpha = sum_k f_k dL/dt_k: the bound scales with sum_k f_k |dL/dt_k|
-    terms = float(np.sum(np.asarray(FIB, dtype=np.float64) * np.abs(ref[5])))
-    assert abs(float(da.item()) - ref[3]) <= tol["dtheta"] * max(terms, abs(ref[3])) + 1e-6
+    _check_grads(got, _oracle_grads(x, f, dtype, rope, **kw), dtype)
 
 
-@pytest.mark.parametrize("dtype,scale", [("bf16", 0.05), ("bf16", 0.3), ("f32", 0.2)])
-def test_explicit_softmax_scale_gradients(dtype, scale):
-    """dQ, dK, dV and dL/dalpha with a caller-given softmax scale."""
+@pytest.mark.parametrize("dtype,scale,rope", [("bf16", 0.05, 1e4), ("bf16", 0.3, 0.0), ("bf16", 0.3, 1e4),
+                                              ("f32", 0.2, 1e4)])
+def test_explicit_softmax_scale_gradients(dtype, scale, rope):
+    """dQ, dK, dV, dL/dalpha and dL/dtheta with a caller-given softmax scale."""
     x, f = draw(2, 150, dtype, layer=62, with_dO=True)
     xd = to_dev(x)
     kw = dict(alpha=0.83, W=12, rungs=FIB, scale=scale)
-    o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], **kw)
-    dq, dk, dv, da, dth = api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse, **kw)
+    o, lse = api.sfa_forward(xd["q"], xd["k"], xd["v"], rope_theta=rope, **kw)
+    got = api.sfa_backward(xd["q"], xd["k"], xd["v"], o, xd["dO"], lse, rope_theta=rope, **kw)
     torch.cuda.synchronize()
-    ref = oracle.backward(f["q"], f["k"], f["v"], f["dO"], W=12, rungs=FIB, alpha=0.83, scale=scale)
-    tol = TOL[dtype]
-    for name, got, want in (("dq", dq, ref[0]), ("dk", dk, ref[1]), ("dv", dv, ref[2])):
-        bound = tol["grad"] * max(1.0, float(np.abs(want).max()))
-        assert max_abs(np64(got), want) <= bound, name
-    terms = float(np.sum(np.asarray(FIB, dtype=np.float64) * np.abs(ref[5])))
-    assert abs(float(da.item()) - ref[3]) <= tol["dtheta"] * max(terms, abs(ref[3])) + 1e-6
+    _check_grads(got, _oracle_grads(x, f, dtype, rope, **kw), dtype)
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])

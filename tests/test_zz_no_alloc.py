@@ -53,3 +53,37 @@ def test_noalloc_rejects_shapes_beyond_its_scratch():
     st = lib.sfa_forward_noalloc(p.ref(), fake, fake, fake, fake, fake, ctypes.c_void_p(0),
                                  ctypes.c_void_p(0), ctypes.c_void_p(0))
     assert st == _lib.SFA_ERR_UNSUPPORTED and api.launch_count() == n0
+
+
+def test_noalloc_largest_accepted_shape():
+    """B * T = 32768 with RoPE: the rotated keys fill the scratch exactly
+    (32768 tokens x 2 heads x 64 x 2 bytes = 8 MiB), and the output is
+    bit-identical to sfa_forward's (the same kernels, another workspace)."""
+    lib = _lib.load()
+    B, T, W, alpha = 32, 1024, 12, 1.13
+    p = api.Params(B, T, W=W, alpha=alpha)
+    assert lib.sfa_forward_workspace_size(p.ref()) == lib.sfa_forward_noalloc_scratch_bytes()
+    x, _ = draw(B, T, "bf16", layer=5)
+    xd = to_dev(x)
+    tab = api.rope_table(T, "cuda")
+    ref_o, ref_l = api.sfa_forward(xd["q"], xd["k"], xd["v"], alpha=alpha, W=W)
+    out = torch.full_like(xd["q"], float("nan"))
+    lse = torch.full((B, T, 8), float("nan"), dtype=torch.float32, device="cuda")
+    st = _noalloc(xd, out, lse, tab, alpha=alpha, W=W, dtype=torch.bfloat16)
+    assert st == _lib.SFA_OK, _lib.strerror(st)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref_o) and torch.equal(lse, ref_l)
+
+
+def test_noalloc_in_contexts_the_caller_created():
+    """A caller that creates its own CUDA contexts (cuCtxCreate) and switches
+    between them: in each context both forwards agree bit for bit, and the
+    scratch address and kernel set-up follow the context (a child process, so
+    that no other context exists in it)."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "_noalloc_ctx_child.py")], capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr
