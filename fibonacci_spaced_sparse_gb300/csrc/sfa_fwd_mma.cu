@@ -705,6 +705,7 @@ size_t fwd_mma_workspace(const LayerArgs& a, bool rope) {
 cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* khat, const void* v,
                                  const float2* rope, void* o, float* lse, const void* k_next, void* khat_next,
                                  unsigned* status, bool pdl, cudaStream_t s) {
+    if (fwd_tc_supported(a)) return launch_fwd_tc(a, q, khat, v, rope, o, lse, k_next, khat_next, status, pdl, s);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

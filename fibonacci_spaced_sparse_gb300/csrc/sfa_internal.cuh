@@ -88,6 +88,13 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
                                  const float2* rope, void* o, float* lse, const void* k_next, void* khat_next,
                                  unsigned* status, bool pdl, cudaStream_t s);
 
+// The tcgen05 forward (windows W <= 16, at most 10 kept rungs); the same
+// arguments as launch_fwd_attention.
+bool fwd_tc_supported(const LayerArgs& a);
+cudaError_t launch_fwd_tc(const LayerArgs& a, const void* q, const void* khat, const void* v, const float2* rope,
+                          void* o, float* lse, const void* k_next, void* khat_next, unsigned* status, bool pdl,
+                          cudaStream_t s);
+
 bool bwd_mma_supported(const LayerArgs& a);
 size_t bwd_mma_workspace(const LayerArgs& a, bool rope);
 cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, const void* v, const void* o,
