@@ -634,12 +634,15 @@ def run_decode(args, rank, world, local):
     def step():
         graph.replay()
 
+    t_warm = time.perf_counter()
     for _ in range(max(3, args.warmup)):
         step()
     barrier(dev)
+    step_s = (time.perf_counter() - t_warm) / max(3, args.warmup)
     steps = max(1, args.steps)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
+        soak(step, step_s, dev)
         barrier(dev)
         start.record(stream)
         for _ in range(steps):
@@ -739,15 +742,18 @@ def run_front_end(args, rank, world, local):
             if ev is not None:
                 ev[3 * l + 2].record(stream)
 
+    t_warm = time.perf_counter()
     for _ in range(max(3, args.warmup)):
         step()
     barrier(dev)
+    step_s = (time.perf_counter() - t_warm) / max(3, args.warmup)
     steps = max(1, args.steps)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 * L)] for _ in range(steps)]
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n0 = api.launch_count()
     with ClockSampler(local) as clk:
+        soak(step, step_s, dev)
         barrier(dev)
+        n0 = api.launch_count()
         start.record(stream)
         for s_ in range(steps):
             step(ev[s_])

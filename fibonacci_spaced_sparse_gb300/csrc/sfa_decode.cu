@@ -62,6 +62,10 @@ decode_kernel(const LayerArgs a, int Tc, const T* __restrict__ q, const T* __res
               T* __restrict__ o, float* __restrict__ lse, unsigned* __restrict__ status) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = blockIdx.x % kHkv, b = blockIdx.x / kHkv;
+    // the next launch may be scheduled now; this one reads its inputs only
+    // once the launch before it has completed
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int i = __ldg(pos + b);
     const size_t qbase = ((size_t)b * kHq + g * kG) * kD + lane;
     if (i < 0 || i >= Tc) {
@@ -258,6 +262,32 @@ __device__ __forceinline__ void unpack_row(const RawRow& R, float (&x)[8], float
     }
 }
 
+// Rows of entry e of a query at position i (ra < 0: no entry; rb < 0: no
+// second row), as the kernel below assigns them.
+__device__ __forceinline__ void entry_rows(const LayerArgs& a, int i, int e, int& ra, int& rb) {
+    const int nwin = min(a.W, i) + 1;
+    ra = rb = -1;
+    if (e < nwin) {
+        ra = i - e;
+        return;
+    }
+    int k = e - nwin;
+    for (int r = 0; r < a.nr; ++r)
+        if (a.r[r].c <= i && k-- == 0) {
+            ra = i - a.r[r].n;
+            rb = a.r[r].t > 0.f ? ra - 1 : -1;
+            return;
+        }
+}
+
+// One 128-byte line of K and one of V of cache row j (head g) into L2.
+__device__ __forceinline__ void prefetch_row(const __nv_bfloat16* kc, const __nv_bfloat16* vc, int b, int Tc, int g,
+                                             int j) {
+    const size_t off = (((size_t)b * Tc + j) * kHkv + g) * kD;
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(kc + off));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(vc + off));
+}
+
 __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
     const LayerArgs a, int Tc, const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ kc,
     const __nv_bfloat16* __restrict__ vc, const int* __restrict__ pos, const float2* __restrict__ rope,
@@ -268,6 +298,21 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
     const int g = blockIdx.x % kHkv, b = blockIdx.x / kHkv;
     const size_t qbase = ((size_t)b * kHq + g * kG) * kD;
     const int c = lane & 3, e = warp * 8 + (lane >> 2);
+    // the next launch may be scheduled now; this one reads its inputs only
+    // once the launch before it has completed.  While it waits, it asks L2 for
+    // the cache rows of its entry at the position it reads now (clamped into
+    // the cache): if the launch before rewrites the position, only these
+    // prefetches go to other rows, and every value used is read after the wait
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (c == 0) {
+        const int ip = min(max(*reinterpret_cast<const volatile int*>(pos + b), 0), Tc - 1);
+        int ra, rb;
+        entry_rows(a, ip, e, ra, rb);
+        if (ra >= 0) prefetch_row(kc, vc, b, Tc, g, ra);
+        if (rb >= 0) prefetch_row(kc, vc, b, Tc, g, rb);
+    }
+    if (threadIdx.x < kG) asm volatile("prefetch.global.L2 [%0];" ::"l"(q + qbase + threadIdx.x * kD));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // the query's chunk c of every head (dimensions 8c .. 8c + 7 and their
     // partners), loaded together with the position; each lane rotates the
     // chunk it scores with itself, so no shared copy and no barrier is needed
@@ -418,20 +463,32 @@ __global__ void __launch_bounds__(kFastThreads) decode_fast_kernel(
 cudaError_t launch_decode(const LayerArgs& a, int Tc, sfa_dtype dt, const void* q, const void* kc,
                           const void* vc, const int* pos, const float2* rope, void* o, float* lse,
                           unsigned* status, cudaStream_t s) {
-    const int blocks = a.B * kHkv;
+    // programmatic dependent launch: the CTAs of this launch may be scheduled
+    // while the launch before it drains (they wait for it before any read),
+    // which hides the gap between back-to-back decode calls
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(a.B * kHkv));
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (dt == SFA_BF16 && a.W + 1 + a.nr <= kFastEntries) {
-        decode_fast_kernel<<<blocks, kFastThreads, 0, s>>>(a, Tc, (const __nv_bfloat16*)q, (const __nv_bfloat16*)kc,
-                                                         (const __nv_bfloat16*)vc, pos, rope, (__nv_bfloat16*)o, lse,
-                                                         status);
-    } else if (dt == SFA_F32)
-        decode_kernel<float><<<blocks, kSplit * 32, 0, s>>>(a, Tc, (const float*)q, (const float*)kc,
-                                                            (const float*)vc, pos, rope, (float*)o, lse,
-                                                            status);
-    else
-        decode_kernel<__nv_bfloat16><<<blocks, kSplit * 32, 0, s>>>(
-            a, Tc, (const __nv_bfloat16*)q, (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, pos, rope,
-            (__nv_bfloat16*)o, lse, status);
-    const cudaError_t e = cudaGetLastError();
+        cfg.blockDim = dim3(kFastThreads);
+        e = cudaLaunchKernelEx(&cfg, decode_fast_kernel, a, Tc, (const __nv_bfloat16*)q, (const __nv_bfloat16*)kc,
+                               (const __nv_bfloat16*)vc, pos, rope, (__nv_bfloat16*)o, lse, status);
+    } else if (dt == SFA_F32) {
+        cfg.blockDim = dim3(kSplit * 32);
+        e = cudaLaunchKernelEx(&cfg, decode_kernel<float>, a, Tc, (const float*)q, (const float*)kc,
+                               (const float*)vc, pos, rope, (float*)o, lse, status);
+    } else {
+        cfg.blockDim = dim3(kSplit * 32);
+        e = cudaLaunchKernelEx(&cfg, decode_kernel<__nv_bfloat16>, a, Tc, (const __nv_bfloat16*)q,
+                               (const __nv_bfloat16*)kc, (const __nv_bfloat16*)vc, pos, rope, (__nv_bfloat16*)o,
+                               lse, status);
+    }
     if (e == cudaSuccess) count_launch();
     return e;
 }
