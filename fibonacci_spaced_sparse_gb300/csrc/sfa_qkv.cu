@@ -37,6 +37,7 @@
 #include "sfa_internal.cuh"
 #include "sfa_mma.cuh"
 #include "sfa_ring.cuh"
+#include "sfa_tc.cuh"
 
 namespace sfa {
 
@@ -83,61 +84,12 @@ struct QkvParams {
     int tiles;          // ceil(M / BM) * kNTiles
 };
 
-// ------------------------------------------------------------ tcgen05 PTX
+// ------------------------------------------------------------ tcgen05
 
-// Shared-memory matrix descriptor of a K-major operand tile in the 128-byte
-// swizzle that TMA writes: start address >> 4 (bits 0-13), leading-dimension
-// offset (unused for this layout, 1), stride between 8-row core-matrix groups
-// = 1024 bytes (bits 32-45), the fixed descriptor version 1 (bits 46-48),
-// layout 2 = 128-byte swizzle (bits 61-63).  Tile bases are 1024-byte
-// aligned; a K step of 16 elements advances the start address by 32 bytes.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
-// Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
-// B bf16 (bits 7-9 and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 at
-// bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void tc_mma(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
-        : "memory");
-}
-
-// The mbarrier gets one arrival once every tcgen05.mma issued so far by this
-// thread has completed.
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&r)[32]) {
-    uint32_t u[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
-          "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15]),
-          "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]), "=r"(u[21]), "=r"(u[22]),
-          "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]), "=r"(u[28]), "=r"(u[29]),
-          "=r"(u[30]), "=r"(u[31])
-        : "r"(taddr));
-#pragma unroll
-    for (int j = 0; j < 32; ++j) r[j] = __uint_as_float(u[j]);
-}
-
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// MMA of one k-step: M = 128 tokens, N = 256 features, both operands K-major
+// bf16 tiles in the 128-byte swizzle (sfa_tc.cuh); a K step of 16 elements
+// advances each descriptor's start address by 32 bytes.
+constexpr uint32_t kIdesc = tc::idesc_bf16(BM, BN, false);
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int c0, int c1, uint32_t bar) {
     asm volatile(
@@ -190,15 +142,11 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_rope_kernel(const __grid_cons
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(const_cast<uint32_t*>(tmem_slot))),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        tc::alloc(smem_u32(const_cast<uint32_t*>(tmem_slot)), kTmemCols);
     }
-    tc_fence_before();
+    tc::fence_before();
     __syncthreads();
-    tc_fence_after();
+    tc::fence_after();
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 0) {
@@ -240,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_rope_kernel(const __grid_cons
                     *abort_flag = 1;
                     break;
                 }
-                tc_fence_after();
+                tc::fence_after();
                 const uint32_t acc = tmem + (uint32_t)(buf * BN);
                 bool ok = true;
                 for (int kb = 0; kb < P.nkb; ++kb, ++kbg) {
@@ -250,17 +198,17 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_rope_kernel(const __grid_cons
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
+                    tc::fence_after();
                     const uint32_t a = stages + (uint32_t)s * kStageBytes;
-                    const uint64_t ad = umma_desc(a), bd = umma_desc(a + kABytes);
+                    const uint64_t ad = tc::desc_kmajor(a), bd = tc::desc_kmajor(a + kABytes);
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k)
-                        tc_mma(acc, ad + (uint64_t)(k * UMMA_K * 2 / 16), bd + (uint64_t)(k * UMMA_K * 2 / 16),
-                               (kb | k) != 0);
-                    tc_commit(bar_empty + 8 * s);  // the stage is free once these have read it
+                        tc::mma_ss(acc, ad + (uint64_t)(k * UMMA_K * 2 / 16), bd + (uint64_t)(k * UMMA_K * 2 / 16),
+                                   kIdesc, (kb | k) != 0);
+                    tc::commit(bar_empty + 8 * s);  // the stage is free once these have read it
                 }
                 // the accumulator is complete once every MMA above has
-                tc_commit(bar_tfull + 8 * buf);
+                tc::commit(bar_tfull + 8 * buf);
                 if (!ok) break;
             }
         }
@@ -277,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_rope_kernel(const __grid_cons
                 break;
             }
             if (*abort_flag) break;
-            tc_fence_after();
+            tc::fence_after();
             const int m0 = (t / kNTiles) * BM, n0 = (t % kNTiles) * BN;
             const int row = lb + lane, m = m0 + row;
             const int pos = m < P.M ? m % P.T : 0;
@@ -291,14 +239,20 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_rope_kernel(const __grid_cons
             }
 #pragma unroll 1
             for (int h = 0; h < BN / kD; ++h) {
-                float x[32], y[32];
+                uint32_t xu[32], yu[32];
                 const uint32_t ta = tmem + ((uint32_t)lb << 16) + (uint32_t)(buf * BN + h * kD);
-                tc_ld32(ta, x);
-                tc_ld32(ta + kPairs, y);
-                tc_wait_ld();
+                tc::ld_x32(ta, xu);
+                tc::ld_x32(ta + kPairs, yu);
+                tc::wait_ld();
+                float x[32], y[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    x[j] = __uint_as_float(xu[j]);
+                    y[j] = __uint_as_float(yu[j]);
+                }
                 if (h == BN / kD - 1) {
                     // every column of this accumulator has been read: hand it back
-                    tc_fence_before();
+                    tc::fence_before();
                     __syncwarp();
                     mbar_arrive_if(bar_tempty + 8 * buf, lane == 0);
                 }
@@ -355,12 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1) qkv_rope_kernel(const __grid_cons
         if (lane == 0) bulk_wait_all();
         if (*abort_flag && lane == 0 && warp == 2 && P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
     }
-    tc_fence_before();
+    tc::fence_before();
     __syncthreads();
     if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
-                     : "memory");
+        tc::fence_after();
+        tc::dealloc(tmem, kTmemCols);
     }
 }
 

@@ -95,7 +95,18 @@ typedef struct {
     const float *rungs;/* HOST pointer to K base offsets f_k (finite, > 0) */
     float alpha;       /* the layer's scalar (finite, > 0) */
     float rope_theta;  /* RoPE base (1e4 in the paper); <= 0: inputs already rotated */
-    float scale;       /* softmax scale; 0 selects 1/sqrt(D) */
+    float scale;       /* softmax scale; 0 selects 1/sqrt(D).  Accuracy with
+                          bf16 and rope_theta > 0: the rotated query and key
+                          rows are rounded to bf16 before they are scored, so
+                          a score s = scale q.k carries an error of up to
+                          about scale |q| |k| 2^-7 (Cauchy-Schwarz bound; the
+                          typical error is about 2^-8 scale |q| |k| / sqrt(D)).
+                          For inputs of unit scale this rounding alone
+                          moves O and LSE by about 0.007 at the default scale
+                          1/8 and by about 0.02 at scale 0.3 (600 query rows
+                          measured); sharper scores (a larger scale or larger
+                          norms) move LSE by up to that bound.  fp32, or bf16
+                          without RoPE, scores the given values exactly. */
     sfa_dtype dtype;   /* element type of Q, K, V, O, dO, dQ, dK, dV */
     int round_offsets; /* 0: d_k as computed (interpolated gather); 1: every d_k
                           rounded to the nearest integer, halves up (the static
