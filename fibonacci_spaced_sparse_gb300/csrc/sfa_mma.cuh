@@ -61,6 +61,41 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// try_wait that may suspend the thread inside the barrier until the phase
+// completes or about `ns` nanoseconds pass (the suspend-time hint), so that a
+// waiting thread issues almost no instructions.
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+constexpr uint32_t kSuspendNs = 1000;  // one suspended try of the sleeping waits
+
+// Bounded wait that sleeps in the barrier between tries; false once kWaitNs
+// have passed or another warp gave up (abort_flag may be null).
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait_for(bar, parity, kSuspendNs)) return true;
+    const unsigned long long t0 = now_ns();
+    for (;;) {
+        if (mbar_try_wait_for(bar, parity, kSuspendNs)) return true;
+        if (abort_flag && *abort_flag) return false;
+        if (now_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+// The same for a whole warp: every lane waits, and the warp goes on together
+// (false on every lane when any lane gave up).
+__device__ __forceinline__ bool warp_wait_sleep(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    const bool ok = mbar_wait_sleep(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }

@@ -63,6 +63,35 @@ __device__ __forceinline__ void mma_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_
         : "memory");
 }
 
+// The same, executed by a whole converged warp: one lane chosen by elect.sync
+// issues, so the operands stay warp-uniform (no per-lane conversion before
+// the issue).
+__device__ __forceinline__ void mma_ss_warp(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_warp(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n setp.ne.b32 p, %4, 0;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// commit by one elected lane of a converged warp (the lane that issued)
+__device__ __forceinline__ void commit_warp(uint32_t bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(bar)
+        : "memory");
+}
+
 // The mbarrier gets one arrival once every tcgen05.mma issued so far by this
 // thread has completed.
 __device__ __forceinline__ void commit(uint32_t bar) {
@@ -86,7 +115,21 @@ __device__ __forceinline__ void dealloc(uint32_t taddr, uint32_t ncols) {
 }
 
 // Loads of consecutive 32-bit columns of this thread's TMEM lane (the warp's
-// quarter); complete after wait_ld.
+// quarter); complete after wait_ld.  The registers are written only then, so
+// every register a load fills goes through hold() after the wait: the empty
+// volatile statement keeps the compiler from moving a use of it above the wait.
+__device__ __forceinline__ void hold(uint32_t& r) { asm volatile("" : "+r"(r)); }
+
+template <int N>
+__device__ __forceinline__ void hold(uint32_t (&r)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) hold(r[i]);
+}
+
+__device__ __forceinline__ void ld_x1(uint32_t taddr, uint32_t& r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+}
+
 __device__ __forceinline__ void ld_x8(uint32_t taddr, uint32_t (&r)[8]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
