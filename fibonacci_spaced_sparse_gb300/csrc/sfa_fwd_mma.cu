@@ -70,7 +70,6 @@ struct FwdParams {
     static constexpr int kQMaps = 1;  // the query slot carries the tile's Q
     static constexpr bool kWinRope = true;  // the window slot carries the tile's RoPE rows
     CUtensorMap qmaps[kQMaps];        // Q [B][T][8][64], box of TQ queries x 4 heads
-    CUtensorMap omap;                 // O [B][T][8][64], box of 2 queries x 4 heads, 128-byte swizzle
     CUtensorMap kmap_w;        // Khat, box of win_rows rows
     CUtensorMap vmap_w;        // V, box of win_rows rows
     CUtensorMap kmap_r[RPG];   // Khat, box of RUNG_ROWS + 2p rows, rung position p
@@ -471,9 +470,10 @@ __device__ __forceinline__ void rung_tile_int(const FwdParams& P, const Smem& S,
 }
 
 // Normalise O^T of the pair at tile offset u and stage it, transposed, in
-// this warp's output buffer (rows (query, head), 128-byte swizzle) for a TMA
-// store; the buffer holds one pair, so the previous store must have read it.
-// The log-sum-exp goes straight out.
+// this warp's output buffer (rows (query, head), 16-byte chunk c of row r at
+// c ^ r); the warp then reads it back so that each 16-byte store covers one
+// query's four heads, 512 contiguous bytes of O.  The log-sum-exp goes
+// straight out.
 __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, int u, uint32_t obuf, const Lane& L,
                                            int lane, Unit& U) {
     const int g8 = lane >> 2, tig = lane & 3;
@@ -491,16 +491,21 @@ __device__ __forceinline__ void store_unit(const FwdParams& P, const Tile& x, in
         r[j][0] = pack_bf16(a.x, a.y);
         r[j][1] = pack_bf16(b.x, b.y);
     }
-    if (lane == 0) bulk_wait_read();
-    __syncwarp();
+    __syncwarp();  // the previous pair's rows have been read back
 #pragma unroll
     for (int jj = 0; jj < 2; ++jj)
         stsm_x4_t(obuf + L.ob[jj], r[2 * jj][0], r[2 * jj][1], r[2 * jj + 1][0], r[2 * jj + 1][1]);
-    fence_proxy_async();
     __syncwarp();
-    if (lane == 0 && x.i0 + u < P.a.T) {
-        tma_store_4d(&P.omap, obuf, 0, x.g * kG, x.i0 + u, x.b);
-        bulk_commit();
+    {
+        const int cc = lane & 7;
+        uint4* dst = reinterpret_cast<uint4*>(P.o + (((size_t)x.b * P.a.T + x.i0 + u) * kHq + x.g * kG) * kD);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int rr = 4 * e + (lane >> 3);  // row (query e, head lane / 8)
+            if (x.i0 + u + e < P.a.T)
+                dst[(size_t)e * (kHq * kD / 8) + (lane >> 3) * (kD / 8) + cc] =
+                    lds_u4(obuf + (uint32_t)rr * ROWB + (uint32_t)(((cc ^ rr) & 7) << 4));
+        }
     }
     if (P.lse) {
         // lanes g8 = 0 hold the sums of query u + tig / 2, heads 2 (tig & 1) + {0, 1}
@@ -609,13 +614,11 @@ __device__ void consumer(const FwdParams& P, const Smem& S, int warp, int lane) 
         for (int k = 0; k < 2; ++k) store_unit(P, x, u0 + 2 * k, obuf, L, lane, U[k]);
         x = next_tile(P, x);
     }
-    if (lane == 0) bulk_wait_all();
     return;
 fail:
     if (lane == 0) {
         *S.abort_flag = 1;
         if (P.status) atomicOr(P.status, SFA_DEVSTAT_WAIT_TIMEOUT);
-        bulk_wait_all();
     }
 }
 
@@ -733,7 +736,7 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) ||
         !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows))
         return cudaErrorInvalidValue;
-    if (!encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) || !encode_out(&P.omap, o, a.B, a.T))
+    if (!encode_heads(&P.qmaps[0], q, a.B, a.T, TQ))
         return cudaErrorInvalidValue;
     for (int p = 0; p < RPG; ++p) {
         const int rows = RUNG_ROWS + 2 * p;
