@@ -62,12 +62,12 @@ struct BwdParams {
     CUtensorMap vmap_w;
     CUtensorMap kmap_r[RPG];
     CUtensorMap vmap_r[RPG];
-    CUtensorMap dqmap;         // dQ [B][T][8][64], box of 2 queries x 4 heads
     CUtensorMap dkred, dvred;  // fp32 accumulators [B][T][2][64], box 32 dims x 16 rows, 128-byte swizzle
     LayerArgs a;
     const __nv_bfloat16* q;
     const __nv_bfloat16* o;
     const __nv_bfloat16* dO;
+    __nv_bfloat16* dq;
     const float* lse;
     const float2* rope;        // nullptr: inputs are used as given
     float* dk_acc;             // [B][T][Hkv][D] fp32, rotated frame
@@ -573,18 +573,24 @@ __device__ void bwd_consumer(const BwdParams& P, const Smem& S, int warp, int la
             mbar_arrive_if(bar_empty_g(S, slot), lane == 0);
             ++gcount;
         }
-        if (lane == 0) bulk_wait_read();
-        __syncwarp();
+        __syncwarp();  // the previous tile's rows have been read back
 #pragma unroll
         for (int k = 0; k < 2; ++k) store_dq(P, x, u0 + 2 * k, k, obuf, L, lane, U[k]);
-        fence_proxy_async();
         __syncwarp();
-        if (lane == 0) {
+        {
+            // read back so that each 16-byte store covers one query's four
+            // heads, 512 contiguous bytes of dQ
+            const int cc = lane & 7, h = lane >> 3;
 #pragma unroll
             for (int k = 0; k < 2; ++k)
-                if (x.i0 + u0 + 2 * k < P.a.T)
-                    tma_store_4d(&P.dqmap, obuf + (uint32_t)(k * 8 * ROWB), 0, x.g * kG, x.i0 + u0 + 2 * k, x.b);
-            bulk_commit();
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int iq = x.i0 + u0 + 2 * k + e, rr = 4 * e + h;
+                    uint4* dst = reinterpret_cast<uint4*>(P.dq + (((size_t)x.b * P.a.T + iq) * kHq + x.g * kG + h) * kD);
+                    if (iq < P.a.T)
+                        dst[cc] = lds_u4(obuf + (uint32_t)(k * 8 * ROWB) + (uint32_t)rr * ROWB +
+                                         (uint32_t)(((cc ^ rr) & 7) << 4));
+                }
         }
         x = nx;
     }
@@ -809,6 +815,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     std::memset(&P, 0, sizeof(P));
     P.a = a;
     P.q = static_cast<const __nv_bfloat16*>(q);
+    P.dq = static_cast<__nv_bfloat16*>(dq);
     P.o = static_cast<const __nv_bfloat16*>(o);
     P.dO = static_cast<const __nv_bfloat16*>(dO);
     P.lse = lse;
@@ -828,7 +835,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
     P.win_slot_bytes = 2 * P.win_region + round1k(TQ * TABB);
     if (!encode_rows(&P.kmap_w, khat, a.B, a.T, P.win_rows) || !encode_rows(&P.vmap_w, v, a.B, a.T, P.win_rows) ||
         !encode_red(&P.dkred, P.dk_acc, a.B, a.T) || !encode_red(&P.dvred, P.dv_acc, a.B, a.T) ||
-        !encode_out(&P.dqmap, dq, a.B, a.T) || !encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) ||
+        !encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) ||
         !encode_heads(&P.qmaps[1], dO, a.B, a.T, TQ) || !encode_heads(&P.qmaps[2], o, a.B, a.T, TQ))
         return cudaErrorInvalidValue;
     for (int p = 0; p < RPG; ++p) {
