@@ -487,6 +487,9 @@ __device__ __forceinline__ void zero_block(uint32_t lane_base, uint32_t b) {
 }
 
 // One tile of the warp's 32 rows (query e = 8 q + lane / 4, head lane % 4).
+// kWide: windows W > 12 (up to 16), whose band spans 24 columns of the warp's
+// window scores; otherwise 20.
+template <bool kWide>
 __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int n, const Tile& x, int q,
                              int lane, int& sc) {
     volatile int* abort_flag = S.abort_flag();
@@ -515,7 +518,8 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
         // the 9 columns 8 q .. 8 q + 8 of its block, with group 0 the 24
         // window columns 8 q .. 8 q + 23
         uint32_t ra[GR][8], rb[GR];
-        uint32_t w16[16], w8[8];
+        constexpr int NWC = kWide ? 24 : 20;  // window columns 8 q .. 8 q + NWC - 1
+        uint32_t w16[16], wt[NWC - 16];
 #pragma unroll
         for (int k = 0; k < GR; ++k)
             if (k < nr) {
@@ -524,7 +528,10 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             }
         if (grp == 0) {
             tc::ld_x16(lb + kColW + 8 * q, w16);
-            tc::ld_x8(lb + kColW + 8 * q + 16, w8);
+            if constexpr (kWide)
+                tc::ld_x8(lb + kColW + 8 * q + 16, wt);
+            else
+                tc::ld_x4(lb + kColW + 8 * q + 16, wt);
         }
         tc::wait_ld();
         float sr[GR];
@@ -558,16 +565,16 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
         bool pv_before = G == 0;
         if (grp == 0) {
             tc::hold(w16);
-            tc::hold(w8);
+            tc::hold(wt);
             // window band: block column c (position i0 - W + c) of this lane is
-            // c = 8 q + u, u = 0..23; the row's entries are u = jj .. jj + W at
-            // positions >= 0
-            float w[24];
+            // c = 8 q + u, u < NWC; the row's entries are u = jj .. jj + W at
+            // positions >= 0 (jj + W < NWC)
+            float w[NWC];
             const int lo = max(jj, P.a.W - x.i0 - 8 * q);
             const int hi = row_ok ? jj + P.a.W : -1;
 #pragma unroll
-            for (int u = 0; u < 24; ++u) {
-                const float v = __uint_as_float(u < 16 ? w16[u] : w8[(u - 16) & 7]);
+            for (int u = 0; u < NWC; ++u) {
+                const float v = __uint_as_float(u < 16 ? w16[u] : wt[(u - 16) % (NWC - 16)]);
                 w[u] = (u >= lo && u <= hi) ? v : -INFINITY;
                 m = fmaxf(m, w[u]);
             }
@@ -575,10 +582,14 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             uint32_t pw[12];
 #pragma unroll
             for (int u = 0; u < 12; ++u) {
-                const float p0 = fast_exp2(__fmaf_rn(w[2 * u], sl2, nm));
-                const float p1 = fast_exp2(__fmaf_rn(w[2 * u + 1], sl2, nm));
-                l += p0 + p1;
-                pw[u] = pack_bf16(p0, p1);
+                if (2 * u < NWC) {
+                    const float p0 = fast_exp2(__fmaf_rn(w[2 * u], sl2, nm));
+                    const float p1 = fast_exp2(__fmaf_rn(w[2 * u + 1], sl2, nm));
+                    l += p0 + p1;
+                    pw[u] = pack_bf16(p0, p1);
+                } else {
+                    pw[u] = 0u;  // columns past the band
+                }
             }
             // window probabilities: bf16 pairs 4 q .. 4 q + 11 of the 24 the
             // window P V reads, zeros in the other three blocks of four
@@ -600,15 +611,17 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
                 const float c = fast_exp2(nm_new - nm);
                 l *= c;
                 nm = nm_new;
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t o[32];
-                    tc::ld_x32(lb + kColO + 32 * half, o);
+                // in chunks of 8 columns: this rare path must not raise the
+                // register count of the common one
+#pragma unroll 1
+                for (int c8 = 0; c8 < kD; c8 += 8) {
+                    uint32_t o[8];
+                    tc::ld_x8(lb + kColO + c8, o);
                     tc::wait_ld();
                     tc::hold(o);
 #pragma unroll
-                    for (int d = 0; d < 32; ++d) o[d] = __float_as_uint(__uint_as_float(o[d]) * c);
-                    tc::st_x32(lb + kColO + 32 * half, o);
+                    for (int d = 0; d < 8; ++d) o[d] = __float_as_uint(__uint_as_float(o[d]) * c);
+                    tc::st_x8(lb + kColO + c8, o);
                 }
             }
         }
@@ -643,7 +656,13 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
     // the output: every P V of the tile has completed.  Each lane packs its row
     if (!warp_wait_sleep(S.bar(B_OFULL), n & 1, abort_flag)) return false;
     tc::fence_after();
-    uint32_t pk[32];
+    // each half of the row (32 columns) is read, normalised, packed and
+    // staged (16-byte chunk c of the row at c ^ (row & 7)) before the next
+    // half is read, so that few registers are live at once.  The warp's 32
+    // rows are 8 queries x 4 heads, and the 4 heads of a query are 512
+    // contiguous bytes of O: the warp then stores one query's 512 bytes per
+    // 16-byte store
+    const uint32_t stage = S.stage(q);
     {
         // row sums are >= 1 on rows that exist (the entry at the maximum contributes 1)
         const float inv = l > 0.f ? fast_rcp(l) : 0.f;
@@ -653,25 +672,27 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             tc::ld_x32(lb + kColO + 32 * half, o);
             tc::wait_ld();
             tc::hold(o);
+            if (half == 1) {
+                // every column of O has been read: hand it back
+                tc::fence_before();
+                __syncwarp();
+                mbar_arrive_if(S.bar(B_OFREE), lane == 0);
+            }
 #pragma unroll
-            for (int d = 0; d < 16; ++d)
-                pk[16 * half + d] = pack_bf16(__uint_as_float(o[2 * d]) * inv, __uint_as_float(o[2 * d + 1]) * inv);
+            for (int c = 0; c < 4; ++c) {
+                const int ch = 4 * half + c;
+                uint32_t w[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    w[u] = pack_bf16(__uint_as_float(o[8 * c + 2 * u]) * inv,
+                                     __uint_as_float(o[8 * c + 2 * u + 1]) * inv);
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)lane * ROWB +
+                                                                              (uint32_t)((ch ^ (lane & 7)) << 4)),
+                             "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                             : "memory");
+            }
         }
     }
-    tc::fence_before();
-    __syncwarp();
-    mbar_arrive_if(S.bar(B_OFREE), lane == 0);
-    // the warp's 32 rows are 8 queries x 4 heads, and the 4 heads of a query
-    // are 512 contiguous bytes of O: each lane writes its row to the staging
-    // buffer (16-byte chunk c at c ^ (row & 7)), then the warp stores one
-    // query's 512 bytes per 16-byte store
-    const uint32_t stage = S.stage(q);
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)lane * ROWB +
-                                                                      (uint32_t)((c ^ (lane & 7)) << 4)),
-                     "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                     : "memory");
     __syncwarp();
     {
         const int nq = min(8, P.a.T - (x.i0 + 8 * q));     // queries of the block inside the sequence
@@ -689,16 +710,18 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
     return true;
 }
 
+template <bool kWide>
 __device__ void softmax(const TcParams& P, const Sm& S, uint32_t tmem, int q, int lane) {
     int sc = 0;
     Tile x;
     for (int n = 0; tile_of(P, S, n, x); ++n)
-        if (!softmax_tile(P, S, tmem, n, x, q, lane, sc)) {
+        if (!softmax_tile<kWide>(P, S, tmem, n, x, q, lane, sc)) {
             if (lane == 0) give_up(P, S);
             break;
         }
 }
 
+template <bool kWide>
 __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_constant__ TcParams P) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -757,7 +780,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
     } else if (warp == 1) {
         mma_issuer(P, S, tmem);
     } else if (warp < kPrepWarp0) {
-        softmax(P, S, tmem, warp & 3, lane);
+        softmax<kWide>(P, S, tmem, warp & 3, lane);
     } else {
         prep(P, S, (int)threadIdx.x - 32 * kPrepWarp0, lane);
     }
@@ -810,11 +833,13 @@ cudaError_t launch_fwd_tc(const LayerArgs& a, const void* q, const void* khat, c
         !ring::encode_rows(&P.vwmap, v, a.B, a.T, NWIN) || !ring::encode_rows(&P.krmap, khat, a.B, a.T, NRB) ||
         !ring::encode_rows(&P.vrmap, v, a.B, a.T, NRB))
         return cudaErrorInvalidValue;
-    static CtxSetting configured[64];
-    if (!ctx_setting_holds(configured[dev & 63], kSmemBytes)) {
-        e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    const bool wide = a.W > 12;
+    auto kernel = wide ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
+    static CtxSetting configured[2][64];  // per variant and device
+    if (!ctx_setting_holds(configured[wide][dev & 63], kSmemBytes)) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
         if (e != cudaSuccess) return e;
-        ctx_setting_done(configured[dev & 63], kSmemBytes);
+        ctx_setting_done(configured[wide][dev & 63], kSmemBytes);
     }
     const int grid = P.ntiles < 2 * sms ? P.ntiles : 2 * sms;
     cudaLaunchConfig_t cfg = {};
@@ -827,7 +852,7 @@ cudaError_t launch_fwd_tc(const LayerArgs& a, const void* q, const void* khat, c
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    e = cudaLaunchKernelEx(&cfg, fwd_tc_kernel, P);
+    e = cudaLaunchKernelEx(&cfg, kernel, P);
     if (e != cudaSuccess) return e;
     count_launch();
     return cudaSuccess;
