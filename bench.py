@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -197,12 +198,21 @@ class ClockSampler:
 FORWARD_SOURCES = ("sfa_fwd_mma.cu", "sfa_ring.cuh", "sfa_mma.cuh", "sfa_internal.cuh", "sfa_api.cu")
 
 
-def kernel_source_digest():
+def code_only(text):
+    """The source with its comments, trailing blanks and empty lines removed,
+    so that a change to a comment leaves the digest as it was."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.split("\n") if line.strip())
+
+
+def kernel_source_digest(sources=FORWARD_SOURCES):
+    """First 16 hex digits of SHA-256 over the code of `sources`, in order."""
     from fibonacci_spaced_sparse_gb300 import build
     h = hashlib.sha256()
-    for name in FORWARD_SOURCES:
-        with open(os.path.join(build.CSRC, name), "rb") as fh:
-            h.update(fh.read())
+    for name in sources:
+        with open(os.path.join(build.CSRC, name), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

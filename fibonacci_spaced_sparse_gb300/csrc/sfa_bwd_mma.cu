@@ -502,7 +502,7 @@ __device__ __forceinline__ void bwd_rung_tile(const BwdParams& P, const Smem& S,
 }
 
 // dQ = R(i)^T dQhat of unit k, staged transposed in this warp's buffer for
-// the TMA store.
+// the warp's coalesced 16-byte stores.
 __device__ __forceinline__ void store_dq(const BwdParams& P, const Tile& x, int u, int k, uint32_t obuf,
                                          const BLane& L, int lane, BUnit& U) {
     const int g8 = lane >> 2, tig = lane & 3;

@@ -34,7 +34,8 @@
 //     One online softmax (base 2, lazy rescale: the running max is raised
 //     only when a score exceeds it by more than 2^8) runs over window and
 //     rung entries; O^T accumulates in registers and is transposed with
-//     stmatrix into a staging buffer that a TMA store writes out.
+//     stmatrix into a staging buffer that the warp writes out with
+//     coalesced 16-byte stores.
 //     In a multi-layer call each consumer warp also rotates, tile by tile,
 //     the next layer's keys at its four positions (the window slot already
 //     holds their RoPE rows), so that no later layer needs launch 1.

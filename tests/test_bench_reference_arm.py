@@ -39,3 +39,14 @@ def test_reference_arm_runs_the_oracle_only():
     line = rec["line"]
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["config"] == rec["config"]
+
+
+def test_source_digest_ignores_comments_only():
+    """The traffic record stays valid across an edit to a comment, and is
+    dropped by any change to the code."""
+    sys.path.insert(0, ROOT)
+    import bench
+    src = "int a = 1; // one\n\n/* block\n   comment */\nint b = 2;   \n"
+    assert bench.code_only(src) == "int a = 1;\nint b = 2;"
+    assert bench.code_only(src.replace("// one", "// the first")) == bench.code_only(src)
+    assert bench.code_only(src.replace("2", "3")) != bench.code_only(src)
