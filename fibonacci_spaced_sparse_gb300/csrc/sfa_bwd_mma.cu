@@ -62,6 +62,7 @@ struct BwdParams {
     CUtensorMap vmap_w;
     CUtensorMap kmap_r[RPG];
     CUtensorMap vmap_r[RPG];
+    CUtensorMap tabmap;        // RoPE table rows of a tile (with RoPE)
     CUtensorMap dkred, dvred;  // fp32 accumulators [B][T][2][64], box 32 dims x 16 rows, 128-byte swizzle
     LayerArgs a;
     const __nv_bfloat16* q;
@@ -233,13 +234,15 @@ __device__ __forceinline__ void start_bunit(const BwdParams& P, const Smem& S, c
     U.D = f2(__shfl_sync(kFull, dpart, 4 * (2 * tig)), __shfl_sync(kFull, dpart, 4 * (2 * tig + 1)));
     if (P.rope) {
         // rotation pairs (m, m + 32): words (s, h) and (s + 2, h) of the thread
-        const uint32_t trow = tab + (uint32_t)(min(u + (g8 >> 2), nq - 1) * TABB);
+        const int pr = min(u + (g8 >> 2), nq - 1);
 #pragma unroll
         for (int s = 0; s < 2; ++s)
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                // pairs m, m + 1: table chunk m / 2 = 8 s + 4 h + tig of row pr
+                // (h flips bit 2 of the swizzled chunk)
                 const int m = 16 * s + 8 * h + 2 * tig;
-                const float4 cs = lds_f4(trow + (uint32_t)(m * 8));
+                const float4 cs = lds_f4((tab + tab_chunk(pr, 8 * s + tig)) ^ (uint32_t)(h << 6));
                 const float2 xv = unpack_bf16(U.qf[s][h]), yv = unpack_bf16(U.qf[s + 2][h]);
                 U.qf[s][h] = rope_x(xv, yv, cs);
                 U.qf[s + 2][h] = rope_y(xv, yv, cs);
@@ -838,6 +841,7 @@ cudaError_t launch_bwd_mma(const LayerArgs& a, const void* q, const void* k, con
         !encode_heads(&P.qmaps[0], q, a.B, a.T, TQ) ||
         !encode_heads(&P.qmaps[1], dO, a.B, a.T, TQ) || !encode_heads(&P.qmaps[2], o, a.B, a.T, TQ))
         return cudaErrorInvalidValue;
+    if (rope && !encode_table(&P.tabmap, rope, a.T)) return cudaErrorInvalidValue;
     for (int p = 0; p < RPG; ++p) {
         const int r = RUNG_ROWS + 2 * p;
         if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, r) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, r))

@@ -75,6 +75,7 @@ struct FwdParams {
     CUtensorMap vmap_w;        // V, box of win_rows rows
     CUtensorMap kmap_r[RPG];   // Khat, box of RUNG_ROWS + 2p rows, rung position p
     CUtensorMap vmap_r[RPG];   // V, same boxes
+    CUtensorMap tabmap;        // RoPE table rows of a tile (with RoPE)
     LayerArgs a;
     const __nv_bfloat16* q;
     const float2* rope;        // nullptr: Q and K are used as given
@@ -194,11 +195,13 @@ __device__ __forceinline__ void start_unit(const FwdParams& P, const Smem& S, in
     if (P.rope) {
         const uint4 x4 = lds_u4(qrow + (uint32_t)((tig ^ g8) << 4));
         const uint4 y4 = lds_u4(qrow + (uint32_t)(((4 + tig) ^ g8) << 4));
-        const uint32_t trow = slot + 2 * P.win_region + (uint32_t)(min(u + (g8 >> 2), nq - 1) * TABB + tig * 64);
+        // table chunks 4 tig + w of the row: w flips the low bits of the
+        // swizzled chunk only
+        const uint32_t trow = slot + 2 * P.win_region + tab_chunk(min(u + (g8 >> 2), nq - 1), 4 * tig);
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
             // pairs m = 8 tig + 2 w + {0, 1}: (cos, sin) of both
-            const float4 cs = lds_f4(trow + (uint32_t)(w * 16));
+            const float4 cs = lds_f4(trow ^ (uint32_t)(w << 4));
             const float2 xv = unpack_bf16(u4_get(x4, w));
             const float2 yv = unpack_bf16(u4_get(y4, w));
             U.qf[w >> 1][w & 1] = rope_x(xv, yv, cs);
@@ -550,11 +553,12 @@ __device__ __forceinline__ void load_next_rows(const FwdParams& P, const Tile& x
 __device__ __forceinline__ void store_next_rows(const FwdParams& P, const Smem& S, const Tile& x, int u0, int lane,
                                                 const NextRows& N) {
     const int r = lane >> 3, c = (lane >> 1) & 3, h = lane & 1;
-    const uint32_t trow = S.win + 2 * P.win_region + (uint32_t)((u0 + r) * TABB + 16 * c);
+    // table chunks 8 h + 4 j + c of row u0 + r: j flips bit 2 of the swizzled chunk
+    const uint32_t trow = S.win + 2 * P.win_region + tab_chunk(u0 + r, 8 * h + c);
     uint32_t xo[2], yo[2];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const float4 cs = lds_f4(trow + (uint32_t)(64 * (2 * h + j)));
+        const float4 cs = lds_f4(trow ^ (uint32_t)(j << 6));
         const float2 xv = unpack_bf16(N.xw[j]), yv = unpack_bf16(N.yw[j]);
         xo[j] = rope_x(xv, yv, cs);
         yo[j] = rope_y(xv, yv, cs);
@@ -739,6 +743,7 @@ cudaError_t launch_fwd_attention(const LayerArgs& a, const void* q, const void* 
         return cudaErrorInvalidValue;
     if (!encode_heads(&P.qmaps[0], q, a.B, a.T, TQ))
         return cudaErrorInvalidValue;
+    if (rope && !encode_table(&P.tabmap, rope, a.T)) return cudaErrorInvalidValue;
     for (int p = 0; p < RPG; ++p) {
         const int rows = RUNG_ROWS + 2 * p;
         if (!encode_rows(&P.kmap_r[p], khat, a.B, a.T, rows) || !encode_rows(&P.vmap_r[p], v, a.B, a.T, rows))

@@ -19,7 +19,8 @@
 // a (LayerArgs), rope, status, ntq, ntiles, step_g, step_tq, step_b, win_rows,
 // win_region, kQMaps (static, >= 1) tile maps qmaps[] of per-query
 // [B][T][8][64] tensors that the query slot carries, and kWinRope (static):
-// whether the window slot also carries the RoPE rows of the tile's queries.
+// whether the window slot also carries the RoPE rows of the tile's queries
+// (then also tabmap, the map of encode_table over the RoPE table).
 #pragma once
 
 #include <cuda.h>
@@ -151,15 +152,16 @@ __device__ __forceinline__ bool load_window(const PP& P, const Smem& S, const Ti
                                             int& kt) {
     if (!mbar_wait(bar_empty_w(S), (wcount & 1) ^ 1, S.abort_flag)) return false;
     const int nq = min(TQ, P.a.T - x.i0);
-    const uint32_t tab_bytes = (PP::kWinRope && P.rope) ? (uint32_t)nq * TABB : 0u;
+    const uint32_t tab_bytes = (PP::kWinRope && P.rope) ? (uint32_t)TQ * TABB : 0u;
     kt = active_rungs(S, P.a.nr, x.i0);
     *S.kt = kt;  // published by the arrive below
     const uint32_t full = bar_full_w(S);
     mbar_arrive_expect_tx(full, 2u * P.win_rows * ROWB + tab_bytes);
     tma_load_4d(S.win, &P.kmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
     tma_load_4d(S.win + P.win_region, &P.vmap_w, 0, x.g, x.i0 - P.a.W, x.b, full);
-    // RoPE rows of the tile's query positions (read by the consumers' Q rotation)
-    if (tab_bytes) bulk_g2s(S.win + 2 * P.win_region, P.rope + (size_t)x.i0 * kPairs, tab_bytes, full);
+    // RoPE rows of the tile's query positions (read by the consumers' Q
+    // rotation), in the layout of tab_chunk; rows past T are zero filled
+    if (tab_bytes) tma_load_4d(S.win + 2 * P.win_region, &P.tabmap, 0, 0, x.i0, 0, full);
     ++wcount;
     return true;
 }
@@ -257,6 +259,16 @@ __device__ __forceinline__ TC lds_tc(uint32_t addr) {
     TC v;
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=f"(v.t), "=r"(v.c) : "r"(addr));
     return v;
+}
+
+// Byte offset, in the window slot's RoPE rows, of 16-byte chunk c (pairs
+// 2 c, 2 c + 1) of tile row p.  A row is two 128-byte lines L = 2 p + c / 8
+// loaded under the 128-byte swizzle (the region is 1024-byte aligned), which
+// stores chunk c % 8 of line L at chunk (c % 8) ^ (L % 8): the lanes of a warp
+// that read the same chunk of neighbouring rows then hit different banks.
+__device__ __forceinline__ uint32_t tab_chunk(int p, int c) {
+    const int line = 2 * p + (c >> 3);
+    return (uint32_t)(line * 128 + ((((c & 7) ^ line) & 7) << 4));
 }
 
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
@@ -381,8 +393,6 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 4-D map over O [B][T][8][64] bf16 (innermost first: d, head, t, b), box of
-// 2 queries x 4 heads, 128-byte swizzle (the staging buffer's layout).
 // 4-D map over a [B][T][8][64] bf16 tensor (innermost first: d, head, t, b),
 // box of `queries` queries x 4 heads, 128-byte swizzle, zero fill outside.
 inline bool encode_heads(CUtensorMap* m, const void* base, int B, int T, int queries) {
@@ -397,6 +407,8 @@ inline bool encode_heads(CUtensorMap* m, const void* base, int B, int T, int que
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 4-D map over O [B][T][8][64] bf16 (innermost first: d, head, t, b), box of
+// 2 queries x 4 heads, 128-byte swizzle (the staging buffer's layout).
 inline bool encode_out(CUtensorMap* m, void* base, int B, int T) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -424,6 +436,21 @@ inline bool encode_rows(CUtensorMap* m, const void* base, int B, int T, int rows
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map over the RoPE table's first T positions, each 32 (cos, sin) pairs of
+// fp32 seen as two 128-byte lines of 32 floats (innermost first: float,
+// line, position, 1), box of TQ positions, 128-byte swizzle: the layout that
+// tab_chunk addresses.
+inline bool encode_table(CUtensorMap* m, const float2* rope, int T) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {32u, 2u, (cuuint64_t)T, 1u};
+    const cuuint64_t strides[3] = {128u, (cuuint64_t)TABB, (cuuint64_t)T * TABB};
+    const cuuint32_t box[4] = {32u, 2u, (cuuint32_t)TQ, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float2*>(rope), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace ring
 }  // namespace sfa
