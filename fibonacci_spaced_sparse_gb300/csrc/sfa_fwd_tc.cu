@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
 
 // The mma.sync kernel (sfa_fwd_mma.cu) is the default: measured on GB300 it
 // is faster for this attention (a model-shape layer, B = 32, T = 1024, W = 12,
-// in a 16-layer call: 33 us against 49 us here).  Each softmax group of this
+// in a 16-layer call: 32-33 us against 49 us here).  Each softmax group of this
 // kernel is a chain of a TMEM load, dependent selects and exponentials and
 // TMEM stores on one warp per lane quarter (about 0.45 us per group of two
 // rungs), and the tile's groups follow one another, so two tiles per SM do
