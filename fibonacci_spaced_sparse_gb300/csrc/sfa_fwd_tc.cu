@@ -120,7 +120,7 @@ static_assert(2 * (kSmemBytes + 1024) <= 233472, "shared memory of two CTAs per 
 enum : uint32_t {
     B_QFULL = 0, B_QREADY = 8 * NQB, B_QEMPTY = 16 * NQB, B_WFULL = 24 * NQB, B_WEMPTY = B_WFULL + 16,
     B_KFULL = B_WEMPTY + 16, B_KEMPTY = B_KFULL + 8 * NKV, B_VFULL = B_KEMPTY + 8 * NKV,
-    B_VEMPTY = B_VFULL + 8 * NKV, B_SFULL = B_VEMPTY + 8 * NKV, B_PFULL = B_SFULL + 16, B_PVDONE = B_PFULL + 16, B_OFULL = B_PVDONE + 8,
+    B_VEMPTY = B_VFULL + 8 * NKV, B_SFULL = B_VEMPTY + 8 * NKV, B_PFULL = B_SFULL + 16, B_PVDONE = B_PFULL + 16, B_OFULL = B_PVDONE + 16,
     B_OFREE = B_OFULL + 8, B_DONE = B_OFREE + 8, H_TMEM = B_DONE + 8, H_ABORT = H_TMEM + 4, H_RUNGS = 256
 };
 static_assert(H_ABORT + 4 <= H_RUNGS && H_RUNGS + SFA_MAX_RUNGS * 12 <= kHdrBytes, "header layout");
@@ -327,7 +327,7 @@ __device__ void mma_issuer(const TcParams& P, const Sm& S, uint32_t tmem) {
                     tc::mma_ts_warp(d, area + NRB * k + 8 * ks, tc::desc_mnmajor(S.vg(vb) + kRungBytes * k + 2048 * ks),
                                kIdescPV, 1);
             tc::commit_warp(S.bar(B_VEMPTY, vb));
-            tc::commit_warp(S.bar(B_PVDONE));
+            tc::commit_warp(S.bar(B_PVDONE, b));
             if (grp + 2 < x.ng) {
                 if (!issue_scores(S, tmem, qa, x, grp + 2, G + 2, abort_flag)) {
                     ok = false;
@@ -559,10 +559,12 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             sr[k] = (row_ok && i >= rk.c) ? v : -INFINITY;
             m = fmaxf(m, sr[k]);
         }
-        // O += P V of the group before (in the other area) is complete once
-        // this phase is: every group waits for it, before a rescale of O or
-        // at its end
-        bool pv_before = G == 0;
+        // The P V of group G - 2, which read this area's probabilities, is
+        // complete: the scores just waited for were committed after it.  The
+        // P V of group G - 1 (the other area) is waited for only before a
+        // rescale of O, on that area's barrier; its next phase (group G + 1)
+        // cannot begin before this warp hands over group G, so the parity
+        // wait is unambiguous however many phases went by unobserved.
         if (grp == 0) {
             tc::hold(w16);
             tc::hold(wt);
@@ -604,8 +606,7 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             // and the sum are rescaled
             const bool need = row_ok && __fmaf_rn(m, sl2, nm) > kLazy;
             if (__any_sync(kFull, need)) {
-                if (!warp_wait_sleep(S.bar(B_PVDONE), (G - 1) & 1, abort_flag)) return false;
-                pv_before = true;
+                if (!warp_wait_sleep(S.bar(B_PVDONE, (G - 1) & 1), ((G - 1) >> 1) & 1, abort_flag)) return false;
                 tc::fence_after();
                 const float nm_new = need ? -m * sl2 : nm;
                 const float c = fast_exp2(nm_new - nm);
@@ -647,7 +648,6 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             zero_block(col, (uint32_t)((q + 2) & 3));
             zero_block(col, (uint32_t)((q + 3) & 3));
         }
-        if (!pv_before && !warp_wait_sleep(S.bar(B_PVDONE), (G - 1) & 1, abort_flag)) return false;
         tc::wait_st();
         tc::fence_before();
         __syncwarp();
@@ -753,7 +753,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
             mbar_init(S.bar(B_SFULL, i), 1);
             mbar_init(S.bar(B_PFULL, i), 4);
         }
-        mbar_init(S.bar(B_PVDONE), 1);
+        for (int i = 0; i < 2; ++i) mbar_init(S.bar(B_PVDONE, i), 1);
         mbar_init(S.bar(B_OFULL), 1);
         mbar_init(S.bar(B_OFREE), 4);
         mbar_init(S.bar(B_DONE), 1);
@@ -796,7 +796,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
 
 // The mma.sync kernel (sfa_fwd_mma.cu) is the default: measured on GB300 it
 // is faster for this attention (a model-shape layer, B = 32, T = 1024, W = 12,
-// in a 16-layer call: 32-33 us against 49 us here).  Each softmax group of this
+// in a 16-layer call: 32 us against 47 us here).  Each softmax group of this
 // kernel is a chain of a TMEM load, dependent selects and exponentials and
 // TMEM stores on one warp per lane quarter (about 0.45 us per group of two
 // rungs), and the tile's groups follow one another, so two tiles per SM do
