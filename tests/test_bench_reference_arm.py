@@ -50,3 +50,17 @@ def test_source_digest_ignores_comments_only():
     assert bench.code_only(src) == "int a = 1;\nint b = 2;"
     assert bench.code_only(src.replace("// one", "// the first")) == bench.code_only(src)
     assert bench.code_only(src.replace("2", "3")) != bench.code_only(src)
+
+
+def test_forward_kernel_label_follows_the_selection(monkeypatch):
+    """The bench line names the forward kernel the library's environment
+    switch selects; the committed DRAM-traffic record belongs to the default
+    kernel only."""
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.delenv("SFA_FORWARD_KERNEL", raising=False)
+    assert bench.forward_kernel() == "fwd_mma_kernel"
+    monkeypatch.setenv("SFA_FORWARD_KERNEL", "tc")
+    assert bench.forward_kernel() == "fwd_tc_kernel"
+    monkeypatch.setenv("SFA_FORWARD_KERNEL", "simple")
+    assert bench.forward_kernel() == "fwd_simple_kernel"
