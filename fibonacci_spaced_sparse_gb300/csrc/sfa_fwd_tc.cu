@@ -285,7 +285,12 @@ __device__ void mma_issuer(const TcParams& P, const Sm& S, uint32_t tmem) {
     int G0 = 0;  // first group of the tile
     Tile x;
     bool ok = true;
-    for (int n = 0; ok && tile_of(P, S, n, x); ++n) {
+    // a tile's descriptor takes a few dependent shared-memory reads (the
+    // kept rungs it uses) and two divisions: the next one is worked out
+    // while the tensor core runs the current tile's first scores, not at the
+    // tile boundary, where its latency would hold back the next scores
+    bool have = tile_of(P, S, 0, x);
+    for (int n = 0; ok && have; ++n) {
         const int qb = n % NQB;
         const uint32_t qa = S.q(qb);
         if (!warp_wait_sleep(S.bar(B_QREADY, qb), (n / NQB) & 1, abort_flag) ||
@@ -302,6 +307,8 @@ __device__ void mma_issuer(const TcParams& P, const Sm& S, uint32_t tmem) {
         for (int j = 0; j < first && ok; ++j) ok = issue_scores(S, tmem, qa, x, j, G0 + j, abort_flag);
         if (!ok) break;
         if (x.ng <= 2) tc::commit_warp(S.bar(B_QEMPTY, qb));
+        Tile xn;
+        const bool more = tile_of(P, S, n + 1, xn);
         for (int grp = 0; grp < x.ng; ++grp) {
             const int G = G0 + grp, b = G & 1, vb = G % NKV;
             if (!warp_wait_sleep(S.bar(B_PFULL, b), (G >> 1) & 1, abort_flag) ||
@@ -338,6 +345,8 @@ __device__ void mma_issuer(const TcParams& P, const Sm& S, uint32_t tmem) {
         }
         if (ok) tc::commit_warp(S.bar(B_OFULL));
         G0 += x.ng;
+        x = xn;
+        have = more;
     }
     if (!ok && (threadIdx.x & 31) == 0) give_up(P, S);
     // TMEM is freed only after every MMA issued has completed
@@ -491,7 +500,7 @@ __device__ __forceinline__ void zero_block(uint32_t lane_base, uint32_t b) {
 // window scores; otherwise 20.
 template <bool kWide>
 __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int n, const Tile& x, int q,
-                             int lane, int& sc) {
+                             int lane, int& sc, Tile& xn, bool& more) {
     volatile int* abort_flag = S.abort_flag();
     const int r = 32 * q + lane;           // MMA row = 4 e + h
     const int e = r >> 2, h = r & 3;       // query offset in the tile, head
@@ -653,6 +662,8 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
         __syncwarp();
         mbar_arrive_if(S.bar(B_PFULL, b), lane == 0);
     }
+    // the next tile's descriptor, while the tile's last P V runs
+    more = tile_of(P, S, n + 1, xn);
     // the output: every P V of the tile has completed.  Each lane packs its row
     if (!warp_wait_sleep(S.bar(B_OFULL), n & 1, abort_flag)) return false;
     tc::fence_after();
@@ -714,11 +725,17 @@ template <bool kWide>
 __device__ void softmax(const TcParams& P, const Sm& S, uint32_t tmem, int q, int lane) {
     int sc = 0;
     Tile x;
-    for (int n = 0; tile_of(P, S, n, x); ++n)
-        if (!softmax_tile<kWide>(P, S, tmem, n, x, q, lane, sc)) {
+    bool have = tile_of(P, S, 0, x);
+    for (int n = 0; have; ++n) {
+        Tile xn;
+        bool more = false;
+        if (!softmax_tile<kWide>(P, S, tmem, n, x, q, lane, sc, xn, more)) {
             if (lane == 0) give_up(P, S);
             break;
         }
+        x = xn;
+        have = more;
+    }
 }
 
 template <bool kWide>
@@ -796,7 +813,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
 
 // The mma.sync kernel (sfa_fwd_mma.cu) is the default: measured on GB300 it
 // is faster for this attention (a model-shape layer, B = 32, T = 1024, W = 12,
-// in a 16-layer call: 32 us against 47 us here).  Each softmax group of this
+// in a 16-layer call: 32 us against 46 us here).  Each softmax group of this
 // kernel is a chain of a TMEM load, dependent selects and exponentials and
 // TMEM stores on one warp per lane quarter (about 0.45 us per group of two
 // rungs), and the tile's groups follow one another, so two tiles per SM do
