@@ -80,13 +80,16 @@ constexpr int kPrepThreads = 64;
 constexpr float kLazy = 8.0f;     // a later group raises the row maximum only past this margin (log2 units)
 
 constexpr int NQB = 2;            // Q buffers: the loads run one tile ahead
-constexpr int NKV = 2;            // rung-group key and value buffers each
+constexpr int NKV = 2;            // rung-group key buffers
+constexpr int NV = 3;             // rung-group value buffers: a group's values load as soon as the
+                                  // P V three groups back has read its buffer, early enough not
+                                  // to hold up its own P V (with two, that reload showed)
 constexpr uint32_t kQBytes = MROWS * ROWB;          // one Q buffer (rows 124..127 stay zero)
 constexpr uint32_t kQBox = TQ * kG * ROWB;          // bytes one Q box moves (zero filled past T)
 constexpr uint32_t kWinTensor = NWIN * ROWB;        // 6 KB: Khat, then V
 constexpr uint32_t kRungBytes = NRB * ROWB;         // 4 KB
 constexpr uint32_t kGroupBytes = GR * kRungBytes;   // 8 KB
-constexpr uint32_t kStageBytes = 32 * ROWB;         // one softmax warp's 32 output rows
+constexpr uint32_t kStageBytes = 32 * ROWB / 2;     // one softmax warp's 32 output rows, half a row each
 
 // TMEM columns of a CTA
 constexpr uint32_t kColW = 0;     // window scores (48), then its probabilities (24 bf16 pairs)
@@ -106,8 +109,8 @@ constexpr uint32_t kHdrBytes = 1024;
 constexpr uint32_t kOffQ = kHdrBytes;
 constexpr uint32_t kOffWin = kOffQ + NQB * kQBytes;
 constexpr uint32_t kOffKg = kOffWin + 4 * kWinTensor;     // [NKV]; the window blocks are [2]
-constexpr uint32_t kOffVg = kOffKg + NKV * kGroupBytes;   // [NKV]
-constexpr uint32_t kOffStage = kOffVg + NKV * kGroupBytes;
+constexpr uint32_t kOffVg = kOffKg + NKV * kGroupBytes;   // [NV]
+constexpr uint32_t kOffStage = kOffVg + NV * kGroupBytes;
 constexpr uint32_t kSmemUsed = kOffStage + 4 * kStageBytes;
 constexpr size_t kSmemBytes = 1024 + (size_t)kSmemUsed;
 static_assert(kOffQ % 1024 == 0 && kOffWin % 1024 == 0 && kOffKg % 1024 == 0 && kOffVg % 1024 == 0 &&
@@ -120,7 +123,7 @@ static_assert(2 * (kSmemBytes + 1024) <= 233472, "shared memory of two CTAs per 
 enum : uint32_t {
     B_QFULL = 0, B_QREADY = 8 * NQB, B_QEMPTY = 16 * NQB, B_WFULL = 24 * NQB, B_WEMPTY = B_WFULL + 16,
     B_KFULL = B_WEMPTY + 16, B_KEMPTY = B_KFULL + 8 * NKV, B_VFULL = B_KEMPTY + 8 * NKV,
-    B_VEMPTY = B_VFULL + 8 * NKV, B_SFULL = B_VEMPTY + 8 * NKV, B_PFULL = B_SFULL + 16, B_PVDONE = B_PFULL + 16, B_OFULL = B_PVDONE + 16,
+    B_VEMPTY = B_VFULL + 8 * NV, B_SFULL = B_VEMPTY + 8 * NV, B_PFULL = B_SFULL + 16, B_PVDONE = B_PFULL + 16, B_OFULL = B_PVDONE + 16,
     B_OFREE = B_OFULL + 8, B_DONE = B_OFREE + 8, H_TMEM = B_DONE + 8, H_ABORT = H_TMEM + 4, H_RUNGS = 256
 };
 static_assert(H_ABORT + 4 <= H_RUNGS && H_RUNGS + SFA_MAX_RUNGS * 12 <= kHdrBytes, "header layout");
@@ -221,7 +224,7 @@ __device__ void loader(const TcParams& P, const Sm& S) {
     Tile x;
     bool failed = false;
     for (int n = 0; !failed && tile_of(P, S, n, x); ++n) {
-        // group G (counted over the CTA's tiles) uses key and value buffers G % NKV
+        // group G (counted over the CTA's tiles) uses key buffer G % NKV and value buffer G % NV
         for (int grp = 0; grp < x.ng; ++grp) {
             const int kb = kl % NKV;
             if (!mbar_wait_sleep(S.bar(B_KEMPTY, kb), (uint32_t)((kl / NKV) & 1) ^ 1u, abort_flag)) {
@@ -230,8 +233,8 @@ __device__ void loader(const TcParams& P, const Sm& S) {
             }
             load_group(P, S, &P.krmap, S.kg(kb), S.bar(B_KFULL, kb), x, grp);
             ++kl;
-            const int vb = vl % NKV;
-            if (!mbar_wait_sleep(S.bar(B_VEMPTY, vb), (uint32_t)((vl / NKV) & 1) ^ 1u, abort_flag)) {
+            const int vb = vl % NV;
+            if (!mbar_wait_sleep(S.bar(B_VEMPTY, vb), (uint32_t)((vl / NV) & 1) ^ 1u, abort_flag)) {
                 failed = true;
                 break;
             }
@@ -246,8 +249,8 @@ __device__ void loader(const TcParams& P, const Sm& S) {
         // ever in flight)
         for (int m = max(0, kl - NKV); m < kl; ++m)
             (void)mbar_wait_sleep(S.bar(B_KFULL, m % NKV), (m / NKV) & 1, nullptr);
-        for (int m = max(0, vl - NKV); m < vl; ++m)
-            (void)mbar_wait_sleep(S.bar(B_VFULL, m % NKV), (m / NKV) & 1, nullptr);
+        for (int m = max(0, vl - NV); m < vl; ++m)
+            (void)mbar_wait_sleep(S.bar(B_VFULL, m % NV), (m / NV) & 1, nullptr);
     }
 }
 
@@ -310,10 +313,10 @@ __device__ void mma_issuer(const TcParams& P, const Sm& S, uint32_t tmem) {
         Tile xn;
         const bool more = tile_of(P, S, n + 1, xn);
         for (int grp = 0; grp < x.ng; ++grp) {
-            const int G = G0 + grp, b = G & 1, vb = G % NKV;
+            const int G = G0 + grp, b = G & 1, vb = G % NV;
             if (!warp_wait_sleep(S.bar(B_PFULL, b), (G >> 1) & 1, abort_flag) ||
                 (grp == 0 && !warp_wait_sleep(S.bar(B_OFREE), (n & 1) ^ 1, abort_flag)) ||
-                !warp_wait_sleep(S.bar(B_VFULL, vb), (G / NKV) & 1, abort_flag)) {
+                !warp_wait_sleep(S.bar(B_VFULL, vb), (G / NV) & 1, abort_flag)) {
                 ok = false;
                 break;
             }
@@ -667,12 +670,13 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
     // the output: every P V of the tile has completed.  Each lane packs its row
     if (!warp_wait_sleep(S.bar(B_OFULL), n & 1, abort_flag)) return false;
     tc::fence_after();
-    // each half of the row (32 columns) is read, normalised, packed and
-    // staged (16-byte chunk c of the row at c ^ (row & 7)) before the next
-    // half is read, so that few registers are live at once.  The warp's 32
-    // rows are 8 queries x 4 heads, and the 4 heads of a query are 512
-    // contiguous bytes of O: the warp then stores one query's 512 bytes per
-    // 16-byte store
+    // Each half of the rows (32 columns, 64 bytes) is read, normalised,
+    // packed, staged and stored before the next half is read, so that few
+    // registers are live and the staging buffer holds half rows: 16-byte
+    // chunk c of row r at c ^ ((r / 2) % 4), which keeps both the staging
+    // writes (a lane per row) and the read-back (four lanes per row) free of
+    // bank conflicts.  The warp's 32 rows are 8 queries x 4 heads; a store
+    // covers the 64-byte halves of 8 rows (2 queries x 4 heads).
     const uint32_t stage = S.stage(q);
     {
         // row sums are >= 1 on rows that exist (the entry at the maximum contributes 1)
@@ -691,32 +695,32 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             }
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const int ch = 4 * half + c;
                 uint32_t w[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     w[u] = pack_bf16(__uint_as_float(o[8 * c + 2 * u]) * inv,
                                      __uint_as_float(o[8 * c + 2 * u + 1]) * inv);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)lane * ROWB +
-                                                                              (uint32_t)((ch ^ (lane & 7)) << 4)),
+                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stage + (uint32_t)lane * (ROWB / 2) +
+                                                                              (uint32_t)((c ^ ((lane >> 1) & 3)) << 4)),
                              "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                              : "memory");
             }
-        }
-    }
-    __syncwarp();
-    {
-        const int nq = min(8, P.a.T - (x.i0 + 8 * q));     // queries of the block inside the sequence
-        const int nrows = (q == 3 ? min(nq, TQ - 24) : nq) * kG;
-        uint4* dst = reinterpret_cast<uint4*>(P.o + (((size_t)x.b * P.a.T + x.i0 + 8 * q) * kHq + x.g * kG) * kD);
-        const int cc = lane & 7;
+            __syncwarp();
+            const int nq = min(8, P.a.T - (x.i0 + 8 * q));     // queries of the block inside the sequence
+            const int nrows = (q == 3 ? min(nq, TQ - 24) : nq) * kG;
+            uint4* dst =
+                reinterpret_cast<uint4*>(P.o + (((size_t)x.b * P.a.T + x.i0 + 8 * q) * kHq + x.g * kG) * kD);
+            const int cc = lane & 3;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            const int rr = 4 * c + (lane >> 3);
-            if (rr < nrows) dst[(size_t)(rr >> 2) * (kHq * kD / 8) + (rr & 3) * 8 + cc] = ring::lds_u4(stage + (uint32_t)rr * ROWB + (uint32_t)((cc ^ (rr & 7)) << 4));
+            for (int k = 0; k < 4; ++k) {
+                const int rr = 8 * k + (lane >> 2);
+                if (rr < nrows)
+                    dst[(size_t)(rr >> 2) * (kHq * kD / 8) + (rr & 3) * 8 + 4 * half + cc] = ring::lds_u4(
+                        stage + (uint32_t)rr * (ROWB / 2) + (uint32_t)((cc ^ ((rr >> 1) & 3)) << 4));
+            }
+            __syncwarp();  // the half has been read back before the next is staged
         }
     }
-    __syncwarp();
     if (P.lse && row_ok) P.lse[((size_t)x.b * P.a.T + i) * kHq + x.g * kG + h] = (__log2f(l) - nm) * kLn2;
     return true;
 }
@@ -763,6 +767,8 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
         for (int i = 0; i < NKV; ++i) {
             mbar_init(S.bar(B_KFULL, i), 1);
             mbar_init(S.bar(B_KEMPTY, i), 1);
+        }
+        for (int i = 0; i < NV; ++i) {
             mbar_init(S.bar(B_VFULL, i), 1);
             mbar_init(S.bar(B_VEMPTY, i), 1);
         }
@@ -813,7 +819,7 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
 
 // The mma.sync kernel (sfa_fwd_mma.cu) is the default: measured on GB300 it
 // is faster for this attention (a model-shape layer, B = 32, T = 1024, W = 12,
-// in a 16-layer call: 32 us against 46 us here).  Each softmax group of this
+// in a 16-layer call: 32 us against 45 us here).  Each softmax group of this
 // kernel is a chain of a TMEM load, dependent selects and exponentials and
 // TMEM stores on one warp per lane quarter (about 0.45 us per group of two
 // rungs), and the tile's groups follow one another, so two tiles per SM do
