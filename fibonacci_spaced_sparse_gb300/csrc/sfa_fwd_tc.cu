@@ -122,8 +122,8 @@ static_assert(2 * (kSmemBytes + 1024) <= 233472, "shared memory of two CTAs per 
 // header: barriers, then the shared words, then the rung table
 enum : uint32_t {
     B_QFULL = 0, B_QREADY = 8 * NQB, B_QEMPTY = 16 * NQB, B_WFULL = 24 * NQB, B_WEMPTY = B_WFULL + 16,
-    B_KFULL = B_WEMPTY + 16, B_KEMPTY = B_KFULL + 8 * NKV, B_VFULL = B_KEMPTY + 8 * NKV,
-    B_VEMPTY = B_VFULL + 8 * NV, B_SFULL = B_VEMPTY + 8 * NV, B_PFULL = B_SFULL + 16, B_PVDONE = B_PFULL + 16, B_OFULL = B_PVDONE + 16,
+    B_KFULL = B_WEMPTY + 16, B_VFULL = B_KFULL + 8 * NKV,
+    B_VEMPTY = B_VFULL + 8 * NV, B_SFULL = B_VEMPTY + 8 * NV, B_PFULL = B_SFULL + 16, B_OFULL = B_PFULL + 16,
     B_OFREE = B_OFULL + 8, B_DONE = B_OFREE + 8, H_TMEM = B_DONE + 8, H_ABORT = H_TMEM + 4, H_RUNGS = 256
 };
 static_assert(H_ABORT + 4 <= H_RUNGS && H_RUNGS + SFA_MAX_RUNGS * 12 <= kHdrBytes, "header layout");
@@ -227,7 +227,10 @@ __device__ void loader(const TcParams& P, const Sm& S) {
         // group G (counted over the CTA's tiles) uses key buffer G % NKV and value buffer G % NV
         for (int grp = 0; grp < x.ng; ++grp) {
             const int kb = kl % NKV;
-            if (!mbar_wait_sleep(S.bar(B_KEMPTY, kb), (uint32_t)((kl / NKV) & 1) ^ 1u, abort_flag)) {
+            // the key buffer is free once the scores that read it are complete
+            // (key buffer kb and score area kb go together: NKV = 2); their
+            // next phase needs the keys this lane has yet to load
+            if (!mbar_wait_sleep(S.bar(B_SFULL, kb), (uint32_t)((kl / NKV) & 1) ^ 1u, abort_flag)) {
                 failed = true;
                 break;
             }
@@ -271,7 +274,6 @@ __device__ __forceinline__ bool issue_scores(const Sm& S, uint32_t tmem, uint32_
         for (int ks = 0; ks < 4; ++ks)
             tc::mma_ss_warp(d, tc::desc_kmajor(qa + 32 * ks), tc::desc_kmajor(S.kg(kb) + 32 * ks), idesc, ks > 0);
     }
-    tc::commit_warp(S.bar(B_KEMPTY, kb));
     tc::commit_warp(S.bar(B_SFULL, b));
     return true;
 }
@@ -337,7 +339,6 @@ __device__ void mma_issuer(const TcParams& P, const Sm& S, uint32_t tmem) {
                     tc::mma_ts_warp(d, area + NRB * k + 8 * ks, tc::desc_mnmajor(S.vg(vb) + kRungBytes * k + 2048 * ks),
                                kIdescPV, 1);
             tc::commit_warp(S.bar(B_VEMPTY, vb));
-            tc::commit_warp(S.bar(B_PVDONE, b));
             if (grp + 2 < x.ng) {
                 if (!issue_scores(S, tmem, qa, x, grp + 2, G + 2, abort_flag)) {
                     ok = false;
@@ -573,10 +574,10 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
         }
         // The P V of group G - 2, which read this area's probabilities, is
         // complete: the scores just waited for were committed after it.  The
-        // P V of group G - 1 (the other area) is waited for only before a
-        // rescale of O, on that area's barrier; its next phase (group G + 1)
-        // cannot begin before this warp hands over group G, so the parity
-        // wait is unambiguous however many phases went by unobserved.
+        // P V of group G - 1 is waited for only before a rescale of O, on the
+        // release of its value buffer; that barrier's next phase (group
+        // G + 2) cannot begin before this warp hands over group G, so the
+        // parity wait is unambiguous however many phases went by unobserved.
         if (grp == 0) {
             tc::hold(w16);
             tc::hold(wt);
@@ -618,7 +619,7 @@ __device__ bool softmax_tile(const TcParams& P, const Sm& S, uint32_t tmem, int 
             // and the sum are rescaled
             const bool need = row_ok && __fmaf_rn(m, sl2, nm) > kLazy;
             if (__any_sync(kFull, need)) {
-                if (!warp_wait_sleep(S.bar(B_PVDONE, (G - 1) & 1), ((G - 1) >> 1) & 1, abort_flag)) return false;
+                if (!warp_wait_sleep(S.bar(B_VEMPTY, (G - 1) % NV), ((G - 1) / NV) & 1, abort_flag)) return false;
                 tc::fence_after();
                 const float nm_new = need ? -m * sl2 : nm;
                 const float c = fast_exp2(nm_new - nm);
@@ -766,7 +767,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
         }
         for (int i = 0; i < NKV; ++i) {
             mbar_init(S.bar(B_KFULL, i), 1);
-            mbar_init(S.bar(B_KEMPTY, i), 1);
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(S.bar(B_VFULL, i), 1);
@@ -776,7 +776,6 @@ __global__ void __launch_bounds__(NTHREADS, 2) fwd_tc_kernel(const __grid_consta
             mbar_init(S.bar(B_SFULL, i), 1);
             mbar_init(S.bar(B_PFULL, i), 4);
         }
-        for (int i = 0; i < 2; ++i) mbar_init(S.bar(B_PVDONE, i), 1);
         mbar_init(S.bar(B_OFULL), 1);
         mbar_init(S.bar(B_OFREE), 4);
         mbar_init(S.bar(B_DONE), 1);
